@@ -1,0 +1,210 @@
+"""MoE expert-parallel layout / dispatch / combine on one GB300 GPU.
+
+A thin binding over the C ABI of ``libep_gb300.so`` (``include/ep_gb300.h``):
+it only checks tensor dtypes/devices, allocates outputs the caller did not
+pass, and marshals pointers and the current CUDA stream.  Every step of the
+path runs in the library's CUDA kernels; there is no CPU fallback.
+
+    lay = ep_get_layout(topk_idx, num_experts, num_ranks)
+    d = ep_dispatch(x, topk_idx, topk_weights, lay, dtype="fp8")
+    out = ep_combine(y, lay, topk_idx, topk_weights)
+
+Expert ``e`` lives on logical rank ``e // (num_experts // num_ranks)``;
+``topk_idx == -1`` means "no selection".
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _native as N
+from ._native import (EP_ERRBIT_BAD_INDEX, EP_ERRBIT_CAPACITY,  # noqa: F401
+                      EP_ERRBIT_TIMEOUT, EP_FP8_GROUP)
+
+__all__ = ["EPError", "Layout", "Dispatched", "ep_layout_workspace_bytes",
+           "ep_get_layout", "ep_dispatch", "ep_combine", "library_path"]
+
+
+class EPError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        super().__init__(message)
+
+
+def library_path() -> str:
+    N.load()
+    return N.LIB_PATH
+
+
+def _check(status: int, fn: str):
+    if status != N.EP_OK:
+        lib = N.load()
+        name = lib.ep_status_str(status).decode()
+        detail = lib.ep_last_error().decode()
+        raise EPError(status, f"{fn}: {name}: {detail}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device) -> C.c_void_p:
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def _want(t: torch.Tensor, name: str, dtype, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def ep_layout_workspace_bytes(num_tokens: int, num_experts: int, num_ranks: int) -> int:
+    return int(N.load().ep_layout_workspace_bytes(num_tokens, num_experts, num_ranks))
+
+
+@dataclass
+class Layout:
+    """Device tensors of one routing's layout (see ``ep_layout_t``)."""
+    num_tokens_per_expert: torch.Tensor  # int32 [E]
+    num_tokens_per_rank: torch.Tensor    # int32 [R]
+    rank_prefix: torch.Tensor            # int32 [R+1]
+    is_token_in_rank: torch.Tensor       # uint8 [T, R]
+    token_slot: torch.Tensor             # int32 [T, R]
+    error_word: torch.Tensor             # int32 [1] (bit flags)
+    workspace: torch.Tensor              # uint8, zero-filled once
+    num_tokens: int
+    num_experts: int
+    num_ranks: int
+
+    @staticmethod
+    def empty(num_tokens: int, num_experts: int, num_ranks: int, device) -> "Layout":
+        dev = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        ws = ep_layout_workspace_bytes(num_tokens, num_experts, num_ranks)
+        return Layout(
+            torch.empty(num_experts, **i32), torch.empty(num_ranks, **i32),
+            torch.empty(num_ranks + 1, **i32),
+            torch.empty((num_tokens, num_ranks), dtype=torch.uint8, device=dev),
+            torch.empty((num_tokens, num_ranks), **i32),
+            torch.zeros(1, **i32),
+            torch.zeros(max(ws, 16), dtype=torch.uint8, device=dev),
+            num_tokens, num_experts, num_ranks)
+
+    def c_struct(self) -> N.ep_layout_t:
+        return N.ep_layout_t(
+            self.num_tokens_per_expert.data_ptr(), self.num_tokens_per_rank.data_ptr(),
+            self.rank_prefix.data_ptr(), self.is_token_in_rank.data_ptr(),
+            self.token_slot.data_ptr(), self.error_word.data_ptr())
+
+    def num_recv(self) -> int:
+        """N, read back to the host (synchronises)."""
+        return int(self.rank_prefix[self.num_ranks].item())
+
+    def errors(self) -> int:
+        """The device error word, read back to the host (synchronises)."""
+        return int(self.error_word.item()) & 0xffffffff
+
+
+def ep_get_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int,
+                  layout: Optional[Layout] = None, stream=None) -> Layout:
+    _want(topk_idx, "topk_idx", torch.int64)
+    T, K = topk_idx.shape
+    dev = topk_idx.device
+    if layout is None:
+        layout = Layout.empty(T, num_experts, num_ranks, dev)
+    elif (layout.num_tokens, layout.num_experts, layout.num_ranks) != (T, num_experts, num_ranks):
+        raise ValueError("layout was allocated for other sizes")
+    st = layout.c_struct()
+    _check(N.load().ep_get_layout(
+        _ptr(topk_idx), T, K, num_experts, num_ranks, C.byref(st),
+        _ptr(layout.workspace), layout.workspace.numel(), _stream(stream, dev)), "ep_get_layout")
+    return layout
+
+
+@dataclass
+class Dispatched:
+    recv_x: torch.Tensor                      # bf16 or float8_e4m3fn [cap, H]
+    recv_x_scales: Optional[torch.Tensor]     # fp32 [cap, H/128] (fp8 only)
+    recv_src_idx: Optional[torch.Tensor]      # int32 [cap]
+    recv_topk_idx: Optional[torch.Tensor]     # int32 [cap, K]
+    recv_topk_weights: Optional[torch.Tensor]  # fp32 [cap, K]
+
+
+def ep_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: Optional[torch.Tensor],
+                layout: Layout, dtype: str = "bf16", recv_capacity: Optional[int] = None,
+                out: Optional[Dispatched] = None, metadata: bool = True,
+                stream=None) -> Dispatched:
+    """Scatter rows of ``x`` (bf16 [T, H]) to their received slots.
+
+    ``dtype`` is "bf16" or "fp8".  Without ``recv_capacity`` the buffers are
+    sized T * min(K, R), which needs no read-back of the layout.
+    """
+    _want(x, "x", torch.bfloat16)
+    dev = x.device
+    _want(topk_idx, "topk_idx", torch.int64, dev)
+    T, H = x.shape
+    K = topk_idx.shape[1]
+    E, R = layout.num_experts, layout.num_ranks
+    fp8 = {"bf16": False, "fp8": True}[dtype]
+    if recv_capacity is None:
+        recv_capacity = out.recv_x.shape[0] if out is not None else T * min(K, R)
+    if out is None:
+        out = Dispatched(
+            torch.empty((recv_capacity, H), dtype=torch.float8_e4m3fn if fp8 else torch.bfloat16, device=dev),
+            torch.empty((recv_capacity, H // EP_FP8_GROUP), dtype=torch.float32, device=dev) if fp8 else None,
+            torch.empty(recv_capacity, dtype=torch.int32, device=dev) if metadata else None,
+            torch.empty((recv_capacity, K), dtype=torch.int32, device=dev) if metadata else None,
+            torch.empty((recv_capacity, K), dtype=torch.float32, device=dev)
+            if metadata and topk_weights is not None else None)
+    if topk_weights is not None:
+        _want(topk_weights, "topk_weights", torch.float32, dev)
+    _want(out.recv_x, "recv_x", torch.float8_e4m3fn if fp8 else torch.bfloat16, dev)
+    if out.recv_x.shape[0] < recv_capacity:
+        raise ValueError("recv_x has fewer rows than recv_capacity")
+    st = layout.c_struct()
+    _check(N.load().ep_dispatch(
+        _ptr(x), T, H, _ptr(topk_idx), _ptr(topk_weights), K, E, R, C.byref(st),
+        N.EP_DTYPE_FP8_E4M3 if fp8 else N.EP_DTYPE_BF16, _ptr(out.recv_x),
+        _ptr(out.recv_x_scales), _ptr(out.recv_src_idx), _ptr(out.recv_topk_idx),
+        _ptr(out.recv_topk_weights), recv_capacity, _stream(stream, dev)), "ep_dispatch")
+    return out
+
+
+def ep_combine(y: torch.Tensor, layout: Layout, topk_idx: Optional[torch.Tensor] = None,
+               topk_weights: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    """out[t] = bf16(sum over ranks r ascending of c[t,r] * y[token_slot[t,r]]).
+
+    Without weights c = 1; with ``topk_idx``/``topk_weights`` c[t,r] is the
+    sum of t's gate weights on rank r.
+    """
+    _want(y, "y", torch.bfloat16)
+    dev = y.device
+    cap, H = y.shape
+    T, R = layout.num_tokens, layout.num_ranks
+    if (topk_idx is None) != (topk_weights is None):
+        raise ValueError("pass both topk_idx and topk_weights, or neither")
+    K = 0
+    if topk_idx is not None:
+        _want(topk_idx, "topk_idx", torch.int64, dev)
+        _want(topk_weights, "topk_weights", torch.float32, dev)
+        K = topk_idx.shape[1]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    _want(out, "out", torch.bfloat16, dev)
+    st = layout.c_struct()
+    _check(N.load().ep_combine(
+        _ptr(y), cap, H, C.byref(st), T, R, _ptr(topk_idx), _ptr(topk_weights), K,
+        layout.num_experts, _ptr(out), _stream(stream, dev)), "ep_combine")
+    return out

@@ -1,0 +1,80 @@
+"""ctypes view of ``libep_gb300.so`` (the C ABI in ``include/ep_gb300.h``).
+
+Loading fails loudly when the library has not been built: there is no
+fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libep_gb300.so")
+
+EP_OK = 0
+EP_ERR_INVALID_ARG = 1
+EP_ERR_UNSUPPORTED = 2
+EP_ERR_CUDA = 3
+
+EP_DTYPE_BF16 = 0
+EP_DTYPE_FP8_E4M3 = 1
+
+EP_ERRBIT_BAD_INDEX = 0x1
+EP_ERRBIT_CAPACITY = 0x2
+EP_ERRBIT_TIMEOUT = 0x4
+
+EP_MAX_RANKS = 64
+EP_MAX_TOPK = 32
+EP_MAX_EXPERTS = 4096
+EP_MAX_HIDDEN = 16384
+EP_FP8_GROUP = 128
+
+
+class ep_layout_t(C.Structure):
+    _fields_ = [
+        ("num_tokens_per_expert", C.c_void_p),
+        ("num_tokens_per_rank", C.c_void_p),
+        ("rank_prefix", C.c_void_p),
+        ("is_token_in_rank", C.c_void_p),
+        ("token_slot", C.c_void_p),
+        ("error_word", C.c_void_p),
+    ]
+
+
+# name -> (restype, argtypes); mirrors include/ep_gb300.h
+_p, _i, _sz = C.c_void_p, C.c_int, C.c_size_t
+_LP = C.POINTER(ep_layout_t)
+SIGNATURES = {
+    "ep_layout_workspace_bytes": (_sz, [_i, _i, _i]),
+    "ep_get_layout": (_i, [_p, _i, _i, _i, _i, _LP, _p, _sz, _p]),
+    "ep_dispatch": (_i, [_p, _i, _i, _p, _p, _i, _i, _i, _LP, _i, _p, _p, _p, _p, _p, _i, _p]),
+    "ep_combine": (_i, [_p, _i, _i, _LP, _i, _i, _p, _p, _i, _i, _p, _p]),
+    "ep_status_str": (C.c_char_p, [_i]),
+    "ep_last_error": (C.c_char_p, []),
+    "ep_abi_version": (_i, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m combine_ep_get_layout_gb300.build` "
+                    "(or __graft_entry__.build()); there is no fallback path")
+            lib = C.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(lib, name)
+                f.restype = res
+                f.argtypes = args
+            if lib.ep_abi_version() != 1:
+                raise RuntimeError("libep_gb300.so ABI version mismatch")
+            _lib = lib
+    return _lib

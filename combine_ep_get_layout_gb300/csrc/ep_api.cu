@@ -1,0 +1,259 @@
+// The C ABI declared in include/ep_gb300.h: argument validation (all on the
+// host, before any CUDA call, so invalid calls fail synchronously and never
+// reach the GPU), per-device property cache, status strings and the
+// per-thread detail message.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "ep_internal.h"
+
+namespace ep {
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ready[kMaxDevices] = {};
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+void clear_error() { g_last_error[0] = '\0'; }
+
+}  // namespace
+
+ep_status_t fail(ep_status_t status, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+ep_status_t cuda_fail(cudaError_t err, const char *what) {
+  return fail(EP_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(err), cudaGetErrorString(err));
+}
+
+const DeviceInfo *current_device_info() {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cuda_fail(e, "cudaGetDevice");
+    return nullptr;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    fail(EP_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> g(g_dev_mu);
+  if (!g_dev_ready[dev]) {
+    DeviceInfo d;
+    d.device = dev;
+    int major = 0, minor = 0, sms = 0, optin = 0, per_sm = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+            cudaSuccess) {
+      cuda_fail(e, "cudaDeviceGetAttribute");
+      return nullptr;
+    }
+    if (major != 10 || minor != 3) {
+      fail(EP_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major,
+           minor);
+      return nullptr;
+    }
+    d.num_sms = sms;
+    d.max_smem_per_block_optin = (size_t)optin;
+    d.smem_per_sm = (size_t)per_sm;
+    g_dev[dev] = d;
+    g_dev_ready[dev] = true;
+  }
+  return &g_dev[dev];
+}
+
+namespace {
+
+ep_status_t check_routing_sizes(const char *fn, int num_topk, int num_experts, int num_ranks) {
+  if (num_topk < 1 || num_topk > EP_MAX_TOPK)
+    return fail(num_topk < 1 ? EP_ERR_INVALID_ARG : EP_ERR_UNSUPPORTED, "%s: num_topk=%d not in [1, %d]", fn,
+                num_topk, EP_MAX_TOPK);
+  if (num_ranks < 1 || num_ranks > EP_MAX_RANKS)
+    return fail(num_ranks < 1 ? EP_ERR_INVALID_ARG : EP_ERR_UNSUPPORTED, "%s: num_ranks=%d not in [1, %d]", fn,
+                num_ranks, EP_MAX_RANKS);
+  if (num_experts < num_ranks || num_experts > EP_MAX_EXPERTS)
+    return fail(num_experts < num_ranks ? EP_ERR_INVALID_ARG : EP_ERR_UNSUPPORTED,
+                "%s: num_experts=%d not in [num_ranks=%d, %d]", fn, num_experts, num_ranks, EP_MAX_EXPERTS);
+  if (num_experts % num_ranks != 0)
+    return fail(EP_ERR_INVALID_ARG, "%s: num_experts=%d is not a multiple of num_ranks=%d", fn, num_experts,
+                num_ranks);
+  return EP_OK;
+}
+
+ep_status_t check_ptr(const char *fn, const char *name, const void *p, size_t align, bool required) {
+  if (p == nullptr) {
+    if (required) return fail(EP_ERR_INVALID_ARG, "%s: %s is NULL", fn, name);
+    return EP_OK;
+  }
+  if (!aligned(p, align)) return fail(EP_ERR_INVALID_ARG, "%s: %s is not %zu-byte aligned", fn, name, align);
+  return EP_OK;
+}
+
+#define EP_CHECK(expr)                   \
+  do {                                   \
+    const ep_status_t _s = (expr);       \
+    if (_s != EP_OK) return _s;          \
+  } while (0)
+
+}  // namespace
+}  // namespace ep
+
+using namespace ep;
+
+extern "C" {
+
+size_t ep_layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks) {
+  if (num_tokens < 0 || num_ranks < 1 || num_ranks > EP_MAX_RANKS) return 0;
+  return layout_workspace_bytes(num_tokens, num_experts, num_ranks);
+}
+
+ep_status_t ep_get_layout(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
+                          int num_ranks, const ep_layout_t *layout, void *workspace, size_t workspace_bytes,
+                          ep_stream_t stream) {
+  static const char *fn = "ep_get_layout";
+  clear_error();
+  if (num_tokens < 0) return fail(EP_ERR_INVALID_ARG, "%s: num_tokens=%d < 0", fn, num_tokens);
+  EP_CHECK(check_routing_sizes(fn, num_topk, num_experts, num_ranks));
+  const bool any = num_tokens > 0;
+  EP_CHECK(check_ptr(fn, "topk_idx", topk_idx, 8, any));
+  if (layout == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: layout is NULL", fn);
+  EP_CHECK(check_ptr(fn, "layout.num_tokens_per_expert", layout->num_tokens_per_expert, 4, true));
+  EP_CHECK(check_ptr(fn, "layout.num_tokens_per_rank", layout->num_tokens_per_rank, 4, true));
+  EP_CHECK(check_ptr(fn, "layout.rank_prefix", layout->rank_prefix, 4, true));
+  EP_CHECK(check_ptr(fn, "layout.is_token_in_rank", layout->is_token_in_rank, 16, any));
+  EP_CHECK(check_ptr(fn, "layout.token_slot", layout->token_slot, 16, any));
+  EP_CHECK(check_ptr(fn, "layout.error_word", layout->error_word, 4, true));
+  EP_CHECK(check_ptr(fn, "workspace", workspace, 16, true));
+  const size_t need = layout_workspace_bytes(num_tokens, num_experts, num_ranks);
+  if (workspace_bytes < need)
+    return fail(EP_ERR_INVALID_ARG, "%s: workspace_bytes=%zu < %zu needed", fn, workspace_bytes, need);
+  return launch_layout(topk_idx, num_tokens, num_topk, num_experts, num_ranks, *layout, workspace,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+ep_status_t ep_dispatch(const void *x, int num_tokens, int hidden, const int64_t *topk_idx,
+                        const float *topk_weights, int num_topk, int num_experts, int num_ranks,
+                        const ep_layout_t *layout, ep_dtype_t dtype, void *recv_x, float *recv_x_scales,
+                        int32_t *recv_src_idx, int32_t *recv_topk_idx, float *recv_topk_weights,
+                        int recv_capacity, ep_stream_t stream) {
+  static const char *fn = "ep_dispatch";
+  clear_error();
+  if (num_tokens < 0) return fail(EP_ERR_INVALID_ARG, "%s: num_tokens=%d < 0", fn, num_tokens);
+  if (dtype != EP_DTYPE_BF16 && dtype != EP_DTYPE_FP8_E4M3)
+    return fail(EP_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)dtype);
+  const bool fp8 = dtype == EP_DTYPE_FP8_E4M3;
+  if (hidden < 1) return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d < 1", fn, hidden);
+  if (hidden > EP_MAX_HIDDEN)
+    return fail(EP_ERR_UNSUPPORTED, "%s: hidden=%d > %d", fn, hidden, EP_MAX_HIDDEN);
+  if (hidden % (fp8 ? EP_FP8_GROUP : 8) != 0)
+    return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d is not a multiple of %d", fn, hidden, fp8 ? EP_FP8_GROUP : 8);
+  EP_CHECK(check_routing_sizes(fn, num_topk, num_experts, num_ranks));
+  if (recv_capacity < 0) return fail(EP_ERR_INVALID_ARG, "%s: recv_capacity=%d < 0", fn, recv_capacity);
+  const bool any = num_tokens > 0;
+  const bool rows = recv_capacity > 0;
+  EP_CHECK(check_ptr(fn, "x", x, 16, any));
+  EP_CHECK(check_ptr(fn, "topk_idx", topk_idx, 8, any));
+  if (layout == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: layout is NULL", fn);
+  EP_CHECK(check_ptr(fn, "layout.token_slot", layout->token_slot, 4, any));
+  EP_CHECK(check_ptr(fn, "layout.error_word", layout->error_word, 4, true));
+  EP_CHECK(check_ptr(fn, "recv_x", recv_x, 16, rows));
+  EP_CHECK(check_ptr(fn, "recv_x_scales", recv_x_scales, 4, fp8 && rows));
+  EP_CHECK(check_ptr(fn, "recv_src_idx", recv_src_idx, 4, false));
+  EP_CHECK(check_ptr(fn, "recv_topk_idx", recv_topk_idx, 4, false));
+  EP_CHECK(check_ptr(fn, "recv_topk_weights", recv_topk_weights, 4, false));
+  EP_CHECK(check_ptr(fn, "topk_weights", topk_weights, 4, any && recv_topk_weights != nullptr));
+  DispatchArgs a;
+  a.x = static_cast<const uint16_t *>(x);
+  a.num_tokens = num_tokens;
+  a.hidden = hidden;
+  a.num_topk = num_topk;
+  a.num_experts = num_experts;
+  a.num_ranks = num_ranks;
+  a.topk_idx = topk_idx;
+  a.topk_weights = topk_weights;
+  a.token_slot = layout->token_slot;
+  a.error_word = layout->error_word;
+  a.fp8 = fp8;
+  a.recv_x = recv_x;
+  a.recv_x_scales = recv_x_scales;
+  a.recv_src_idx = recv_src_idx;
+  a.recv_topk_idx = recv_topk_idx;
+  a.recv_topk_weights = recv_topk_weights;
+  a.recv_capacity = recv_capacity;
+  return launch_dispatch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ep_status_t ep_combine(const void *y, int recv_capacity, int hidden, const ep_layout_t *layout,
+                       int num_tokens, int num_ranks, const int64_t *topk_idx, const float *topk_weights,
+                       int num_topk, int num_experts, void *out, ep_stream_t stream) {
+  static const char *fn = "ep_combine";
+  clear_error();
+  if (num_tokens < 0) return fail(EP_ERR_INVALID_ARG, "%s: num_tokens=%d < 0", fn, num_tokens);
+  if (recv_capacity < 0) return fail(EP_ERR_INVALID_ARG, "%s: recv_capacity=%d < 0", fn, recv_capacity);
+  if (hidden < 1) return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d < 1", fn, hidden);
+  if (hidden > EP_MAX_HIDDEN)
+    return fail(EP_ERR_UNSUPPORTED, "%s: hidden=%d > %d", fn, hidden, EP_MAX_HIDDEN);
+  if (hidden % 8 != 0) return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d is not a multiple of 8", fn, hidden);
+  if (num_ranks < 1 || num_ranks > EP_MAX_RANKS)
+    return fail(num_ranks < 1 ? EP_ERR_INVALID_ARG : EP_ERR_UNSUPPORTED, "%s: num_ranks=%d not in [1, %d]",
+                fn, num_ranks, EP_MAX_RANKS);
+  const bool weighted = topk_weights != nullptr;
+  if ((topk_idx == nullptr) != (topk_weights == nullptr))
+    return fail(EP_ERR_INVALID_ARG, "%s: topk_idx and topk_weights must both be given or both be NULL", fn);
+  const bool any = num_tokens > 0;
+  if (weighted) {
+    EP_CHECK(check_routing_sizes(fn, num_topk, num_experts, num_ranks));
+    EP_CHECK(check_ptr(fn, "topk_idx", topk_idx, 8, any));
+    EP_CHECK(check_ptr(fn, "topk_weights", topk_weights, 4, any));
+  }
+  EP_CHECK(check_ptr(fn, "y", y, 16, recv_capacity > 0 && any));
+  if (layout == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: layout is NULL", fn);
+  EP_CHECK(check_ptr(fn, "layout.token_slot", layout->token_slot, 4, any));
+  EP_CHECK(check_ptr(fn, "layout.error_word", layout->error_word, 4, true));
+  EP_CHECK(check_ptr(fn, "out", out, 16, any));
+  CombineArgs a;
+  a.y = static_cast<const uint16_t *>(y);
+  a.recv_capacity = recv_capacity;
+  a.hidden = hidden;
+  a.num_tokens = num_tokens;
+  a.num_ranks = num_ranks;
+  a.num_topk = weighted ? num_topk : 0;
+  a.num_experts = weighted ? num_experts : num_ranks;
+  a.token_slot = layout->token_slot;
+  a.error_word = layout->error_word;
+  a.topk_idx = topk_idx;
+  a.topk_weights = topk_weights;
+  a.out = static_cast<uint16_t *>(out);
+  return launch_combine(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char *ep_status_str(ep_status_t status) {
+  switch (status) {
+    case EP_OK: return "EP_OK";
+    case EP_ERR_INVALID_ARG: return "EP_ERR_INVALID_ARG";
+    case EP_ERR_UNSUPPORTED: return "EP_ERR_UNSUPPORTED";
+    case EP_ERR_CUDA: return "EP_ERR_CUDA";
+  }
+  return "EP_STATUS_UNKNOWN";
+}
+
+const char *ep_last_error(void) { return g_last_error; }
+
+int ep_abi_version(void) { return EP_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,223 @@
+/*
+ * ep_gb300.h -- C ABI of the single-GPU MoE expert-parallel hot path:
+ * layout, dispatch (bf16 or fused fp8) and combine, for NVIDIA GB300 (sm_103a).
+ *
+ * The method is the one of TileScale PR #68 "[Example] EP v2 intranode
+ * dispatch/combine" (PR summary and README section "Design"): dispatch is a
+ * count phase that deduplicates each (token, destination rank) pair, a count
+ * exchange that gives every destination a base, and a scatter that writes
+ * every row straight to its final compact index; combine reduces, per source
+ * token, the rows that token was sent as.  Here the expert-parallel ranks are
+ * logical partitions of the expert set inside one GPU's memory, so the count
+ * exchange becomes a device-wide prefix scan and the scatter/gather are
+ * ordinary HBM traffic.
+ *
+ * Conventions shared by every call
+ *   - All array arguments are DEVICE pointers, allocated and owned by the
+ *     caller, row-major, and must stay alive until the stream has passed the
+ *     call.  The library allocates nothing, frees nothing, never synchronises
+ *     the device or the stream, and keeps no state between calls beyond
+ *     per-device launch parameters (SM count, occupancy) cached on first use.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).
+ *   - Sizes: T tokens, K top-k slots, E experts, R logical ranks, H hidden,
+ *     N = number of dispatched rows = sum of per-rank token counts.
+ *     Expert e belongs to rank floor(e / (E/R)); E % R must be 0.
+ *   - topk_idx is int64 [T, K]; -1 means "no selection" (TileScale PR #68,
+ *     commit message on the masked-topk case).  Any other value outside
+ *     [0, E) is treated as -1 and sets EP_ERRBIT_BAD_INDEX in the layout's
+ *     error word.
+ *   - Host-detectable problems (null or misaligned pointers, sizes out of
+ *     range) are reported synchronously by the return value, before anything
+ *     is enqueued.  Data-dependent problems never trap and never hang the GPU:
+ *     they set bits in the layout's device error word.
+ *   - Pointers to arrays that kernels move with 16-byte vectors or bulk copies
+ *     (x, recv_x, y, out, token_slot) must be 16-byte aligned.
+ */
+#ifndef EP_GB300_H
+#define EP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *ep_stream_t;
+
+typedef enum {
+    EP_OK = 0,
+    EP_ERR_INVALID_ARG = 1,  /* a pointer, size or alignment is invalid   */
+    EP_ERR_UNSUPPORTED = 2,  /* valid, but beyond this library's limits   */
+    EP_ERR_CUDA = 3          /* a CUDA runtime call or launch failed      */
+} ep_status_t;
+
+typedef enum {
+    EP_DTYPE_BF16 = 0,       /* received rows are bit copies of x          */
+    EP_DTYPE_FP8_E4M3 = 1    /* received rows are e4m3 codes + fp32 scales */
+} ep_dtype_t;
+
+/* Bits of the device error word (ep_layout_t.error_word). */
+#define EP_ERRBIT_BAD_INDEX 0x1u  /* a topk_idx entry outside [-1, E)        */
+#define EP_ERRBIT_CAPACITY 0x2u   /* a row's slot >= recv_capacity: skipped  */
+#define EP_ERRBIT_TIMEOUT 0x4u    /* a bounded device wait gave up           */
+
+/* Limits of this implementation (EP_ERR_UNSUPPORTED beyond them). */
+#define EP_MAX_RANKS 64
+#define EP_MAX_TOPK 32
+#define EP_MAX_EXPERTS 4096
+#define EP_MAX_HIDDEN 16384
+#define EP_FP8_GROUP 128          /* elements per fp8 scale */
+
+/*
+ * The layout of one routing (the output of ep_get_layout, the input of
+ * ep_dispatch and ep_combine).  All members are caller-allocated device
+ * pointers:
+ *   num_tokens_per_expert [E]   int32: valid selections of each expert.
+ *   num_tokens_per_rank   [R]   int32: tokens sent to each rank (a token
+ *                               counts once per rank however many of its
+ *                               experts live there).
+ *   rank_prefix           [R+1] int32: exclusive prefix sum of the above;
+ *                               rank r's received rows are
+ *                               [rank_prefix[r], rank_prefix[r+1]) and
+ *                               rank_prefix[R] = N.
+ *   is_token_in_rank      [T*R] uint8: 1 if token t is sent to rank r.
+ *   token_slot            [T*R] int32: the received row of (t, r), or -1.
+ *                               Rows of one rank are in ascending token
+ *                               order (a stable scatter).
+ *   error_word            [1]   uint32: EP_ERRBIT_* flags.  ep_get_layout
+ *                               clears it; ep_dispatch and ep_combine given
+ *                               this layout OR their bits into it.
+ * The layout is the single-GPU counterpart of the count matrix and
+ * send_base[d] + slot of TileScale PR #68 (README section "Design").
+ */
+typedef struct {
+    int32_t *num_tokens_per_expert;
+    int32_t *num_tokens_per_rank;
+    int32_t *rank_prefix;
+    uint8_t *is_token_in_rank;
+    int32_t *token_slot;
+    uint32_t *error_word;
+} ep_layout_t;
+
+/*
+ * Bytes of device workspace ep_get_layout needs for these sizes.  The
+ * workspace must be zero-filled once when it is allocated; every call
+ * leaves it zeroed again on exit, so it can be reused by later calls with
+ * any sizes up to the ones it was sized for.  Calls sharing one workspace
+ * must be ordered (the same stream, or events).
+ */
+size_t ep_layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
+
+/*
+ * Layout: the count phase and the count exchange of TileScale PR #68
+ * (README section "Design"; commit message on do_expand: "phase 1 tallies
+ * per destination, phase 2 turns tallies into a base, phase 3 adds a
+ * locally-claimed slot"), on one GPU.  One cooperative kernel: each block
+ * counts its tokens' experts (shared-memory atomics) and ranks (warp
+ * ballots, one bit per (token, rank) however many experts map there),
+ * publishes per-rank block totals, waits at a bounded grid barrier, then
+ * derives each rank's base by an exclusive scan and writes token_slot.
+ *
+ *   topk_idx  [T*K] int64, device.
+ *   T >= 0 (T == 0 writes zero counts), 1 <= K <= EP_MAX_TOPK,
+ *   1 <= R <= EP_MAX_RANKS, R <= E <= EP_MAX_EXPERTS, E % R == 0.
+ *   layout    every member non-null (token_slot 16-byte aligned).
+ *   workspace >= ep_layout_workspace_bytes(T, E, R) bytes, zero-filled at
+ *             allocation (see above), 16-byte aligned.
+ */
+ep_status_t ep_get_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
+                          int num_experts, int num_ranks,
+                          const ep_layout_t *layout, void *workspace,
+                          size_t workspace_bytes, ep_stream_t stream);
+
+/*
+ * Dispatch: the scatter phase of TileScale PR #68 (PR summary: rows go
+ * straight to their final compact index, no copy epilogue), with the fp8
+ * cast of DeepEP's per_token_cast_to_fp8 layout fused into the same pass
+ * (same page, commit message on packing the fp8 row: per-token,
+ * per-128-element fp32 scales; no separate scale transfer).  Each token's
+ * row is read once and written to every rank it is sent to.
+ *
+ *   x            [T*H] bf16 (uint16 bit patterns), device, 16-byte aligned.
+ *   topk_idx     [T*K] int64 and topk_weights [T*K] fp32, device: the same
+ *                routing ep_get_layout saw (topk_weights may be NULL only if
+ *                recv_topk_weights is NULL).
+ *   layout       from ep_get_layout on this routing.
+ *   dtype        EP_DTYPE_BF16: recv_x is bf16 [recv_capacity*H];
+ *                  H % 8 == 0.
+ *                EP_DTYPE_FP8_E4M3: recv_x is e4m3 [recv_capacity*H] and
+ *                  recv_x_scales fp32 [recv_capacity*(H/128)]; H % 128 == 0.
+ *                  Per 128-element group: amax = max|x|,
+ *                  scale = amax / 448 (fp32, round to nearest even),
+ *                  code = e4m3(x / scale) rounded to nearest even and
+ *                  saturated to +-448; an all-zero group has scale 0.
+ *   recv_src_idx      [recv_capacity] int32: source token of each row.
+ *   recv_topk_idx     [recv_capacity*K] int32: local expert (e - r*E/R) of
+ *                     each top-k slot whose expert is on the row's rank r,
+ *                     else -1 (same page, commit message adding cumulative
+ *                     recv stats: recv_topk_idx holds the local expert).
+ *   recv_topk_weights [recv_capacity*K] fp32: the gate weight where
+ *                     recv_topk_idx != -1, else 0.
+ *   The three metadata outputs may each be NULL (not written).
+ *   recv_capacity >= 0: rows whose slot >= recv_capacity are skipped and set
+ *                EP_ERRBIT_CAPACITY; T*min(K,R) always suffices.
+ *   Rows [N, recv_capacity) are not written.
+ *   1 <= H <= EP_MAX_HIDDEN.
+ */
+ep_status_t ep_dispatch(const void *x, int num_tokens, int hidden,
+                        const int64_t *topk_idx, const float *topk_weights,
+                        int num_topk, int num_experts, int num_ranks,
+                        const ep_layout_t *layout, ep_dtype_t dtype,
+                        void *recv_x, float *recv_x_scales,
+                        int32_t *recv_src_idx, int32_t *recv_topk_idx,
+                        float *recv_topk_weights, int recv_capacity,
+                        ep_stream_t stream);
+
+/*
+ * Combine: the local reduce of TileScale PR #68 (PR summary: one block per
+ * source token reduces the rows stored back for it).  On one GPU the
+ * store-back slot comm_x[rank][src_token] is the received row
+ * token_slot[t][r] itself, so combine gathers straight from the expert
+ * stage's output:
+ *
+ *   out[t] = bf16( sum over r = 0..R-1 ascending with token_slot[t][r] >= 0
+ *                  of c[t][r] * y[token_slot[t][r]] )
+ *
+ * accumulated in fp32 with separate multiply and add, rounded to nearest
+ * even at the end.  c = 1 when topk_weights is NULL (the pages' combine);
+ * otherwise c[t][r] is the fp32 sum, in k order, of the weights of t's
+ * experts on rank r.  A token sent nowhere combines to +0 (same page,
+ * commit message on the masked-topk case).
+ *
+ *   y        [recv_capacity*H] bf16, device, 16-byte aligned: row s is the
+ *            expert output for received row s.  Rows with
+ *            token_slot >= recv_capacity are skipped (EP_ERRBIT_CAPACITY).
+ *   layout   the layout the rows were dispatched with.
+ *   topk_idx, topk_weights: [T*K] device, or both NULL for the plain sum.
+ *   out      [T*H] bf16, device, 16-byte aligned.  H % 8 == 0.
+ */
+ep_status_t ep_combine(const void *y, int recv_capacity, int hidden,
+                       const ep_layout_t *layout, int num_tokens, int num_ranks,
+                       const int64_t *topk_idx, const float *topk_weights,
+                       int num_topk, int num_experts, void *out,
+                       ep_stream_t stream);
+
+/* A static, human-readable name of a status. */
+const char *ep_status_str(ep_status_t status);
+
+/* The detail message of the last failing call on this host thread ("" if
+ * none).  Valid until the next call on the same thread. */
+const char *ep_last_error(void);
+
+/* ABI version of this header: bumped on any incompatible change. */
+#define EP_ABI_VERSION 1
+int ep_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_GB300_H */

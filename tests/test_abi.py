@@ -1,0 +1,154 @@
+"""The C-ABI library builds, loads and exports every function the public
+header declares; invalid arguments are rejected on the host, synchronously,
+before any CUDA call (so these run without a GPU; no compute call is made)."""
+import ctypes as C
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from combine_ep_get_layout_gb300 import build, _native
+    build.build()
+    return _native.load()
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_]\w*\s*\*?\s*(ep_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("ep_get_layout", "ep_dispatch", "ep_combine", "ep_layout_workspace_bytes"):
+        assert required in names
+
+
+@pytest.mark.parametrize("name", declared_functions())
+def test_symbol_exported(lib, name):
+    assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_bindings_cover_header():
+    from combine_ep_get_layout_gb300 import _native
+    assert set(declared_functions()) == set(_native.SIGNATURES)
+
+
+def test_constants_match_header():
+    from combine_ep_get_layout_gb300 import _native
+    text = "".join(open(h).read() for h in HEADERS)
+    for name, value in re.findall(r"#define\s+(EP_[A-Z0-9_]+)\s+(0x[0-9a-fA-F]+|\d+)u?", text):
+        if hasattr(_native, name):
+            assert getattr(_native, name) == int(value, 0), name
+    for name, value in re.findall(r"\b(EP_(?:OK|ERR_\w+|DTYPE_\w+))\s*=\s*(\d+)", text):
+        assert getattr(_native, name) == int(value), name
+
+
+def test_workspace_bytes(lib):
+    a = lib.ep_layout_workspace_bytes(8192, 256, 8)
+    b = lib.ep_layout_workspace_bytes(65536, 256, 8)
+    assert a > 0 and b > a and a % 256 == 0
+    assert lib.ep_layout_workspace_bytes(0, 16, 4) > 0
+    assert lib.ep_layout_workspace_bytes(-1, 16, 4) == 0
+    assert lib.ep_layout_workspace_bytes(10, 16, 0) == 0
+
+
+def _layout(base=0x10000):
+    from combine_ep_get_layout_gb300._native import ep_layout_t
+    return ep_layout_t(base, base + 0x100, base + 0x200, base + 0x400, base + 0x800, base + 0x1000)
+
+
+def _status(lib, s):
+    return lib.ep_status_str(s).decode(), lib.ep_last_error().decode()
+
+
+FAKE = C.c_void_p(0x20000)     # never dereferenced: validation fails first
+MISALIGNED = C.c_void_p(0x20004)
+
+
+@pytest.mark.parametrize("kw,needle", [
+    (dict(idx=None), "topk_idx is NULL"),
+    (dict(T=-1), "num_tokens"),
+    (dict(K=0), "num_topk"),
+    (dict(R=0), "num_ranks"),
+    (dict(E=12, R=8), "multiple"),
+    (dict(E=4, R=8), "num_experts"),
+    (dict(ws_bytes=16), "workspace_bytes"),
+    (dict(ws=None), "workspace is NULL"),
+    (dict(idx=C.c_void_p(0x20004 + 2)), "aligned"),
+    (dict(layout_none=True), "layout is NULL"),
+])
+def test_get_layout_rejects(lib, kw, needle):
+    args = dict(idx=FAKE, T=100, K=4, E=16, R=4, ws=FAKE, ws_bytes=1 << 20, layout_none=False)
+    args.update(kw)
+    lay = None if args["layout_none"] else C.byref(_layout())
+    s = lib.ep_get_layout(args["idx"], args["T"], args["K"], args["E"], args["R"], lay,
+                          args["ws"], args["ws_bytes"], None)
+    name, msg = _status(lib, s)
+    assert name == "EP_ERR_INVALID_ARG", (name, msg)
+    assert needle in msg
+
+
+def test_limits_are_unsupported_not_invalid(lib):
+    s = lib.ep_get_layout(FAKE, 10, 4, 4096 * 2, 128, C.byref(_layout()), FAKE, 1 << 20, None)
+    assert _status(lib, s)[0] == "EP_ERR_UNSUPPORTED"
+    s = lib.ep_get_layout(FAKE, 10, 33, 64, 8, C.byref(_layout()), FAKE, 1 << 20, None)
+    assert _status(lib, s)[0] == "EP_ERR_UNSUPPORTED"
+
+
+@pytest.mark.parametrize("kw,needle", [
+    (dict(H=100), "multiple of 8"),
+    (dict(H=256 + 8, dtype=1), "multiple of 128"),
+    (dict(dtype=7), "dtype"),
+    (dict(x=None), "x is NULL"),
+    (dict(x=MISALIGNED), "x is not 16-byte aligned"),
+    (dict(cap=-1), "recv_capacity"),
+    (dict(recv_x=None), "recv_x is NULL"),
+    (dict(dtype=1, scales=None), "recv_x_scales is NULL"),
+    (dict(w=None), "topk_weights is NULL"),
+    (dict(H=0), "hidden"),
+])
+def test_dispatch_rejects(lib, kw, needle):
+    a = dict(x=FAKE, T=100, H=256, idx=FAKE, w=FAKE, K=4, E=16, R=4, dtype=0, recv_x=FAKE,
+             scales=FAKE, src=FAKE, ridx=FAKE, rw=FAKE, cap=400)
+    a.update(kw)
+    s = lib.ep_dispatch(a["x"], a["T"], a["H"], a["idx"], a["w"], a["K"], a["E"], a["R"],
+                        C.byref(_layout()), a["dtype"], a["recv_x"], a["scales"], a["src"],
+                        a["ridx"], a["rw"], a["cap"], None)
+    name, msg = _status(lib, s)
+    assert name == "EP_ERR_INVALID_ARG", (name, msg)
+    assert needle in msg
+
+
+@pytest.mark.parametrize("kw,needle", [
+    (dict(idx=None), "both"),
+    (dict(H=12), "multiple of 8"),
+    (dict(out=None), "out is NULL"),
+    (dict(y=MISALIGNED), "y is not 16-byte aligned"),
+    (dict(R=0), "num_ranks"),
+    (dict(E=10), "multiple"),
+])
+def test_combine_rejects(lib, kw, needle):
+    a = dict(y=FAKE, cap=400, H=256, T=100, R=4, idx=FAKE, w=FAKE, K=4, E=16, out=FAKE)
+    a.update(kw)
+    s = lib.ep_combine(a["y"], a["cap"], a["H"], C.byref(_layout()), a["T"], a["R"], a["idx"],
+                       a["w"], a["K"], a["E"], a["out"], None)
+    name, msg = _status(lib, s)
+    assert name == "EP_ERR_INVALID_ARG", (name, msg)
+    assert needle in msg
+
+
+def test_status_strings(lib):
+    assert [lib.ep_status_str(i).decode() for i in range(4)] == [
+        "EP_OK", "EP_ERR_INVALID_ARG", "EP_ERR_UNSUPPORTED", "EP_ERR_CUDA"]
+    assert lib.ep_abi_version() == 1

@@ -1,0 +1,67 @@
+"""Back-to-back calls on the same buffers: every call gives the first call's
+answer, no received row is duplicated, and the error word stays clear.
+Races in a layout/dispatch/combine path tend to show only after many calls
+(TileScale PR #68, README section "Testing": the compact list is checked for
+duplicate (src_rank, src_token) pairs after thousands of back-to-back calls)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+ep = pytest.importorskip("combine_ep_get_layout_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from combine_ep_get_layout_gb300 import build
+    build.build()
+
+
+import gpu_util as U  # noqa: E402
+
+
+@pytest.mark.parametrize("name,calls", [("bf16_4096x4096_top6_64e", 1000),
+                                        ("skew_bf16_4096x4096_top6_64e_zipf1.2_mask10", 500),
+                                        ("fp8_8192x7168_top8_256e", 300)])
+def test_repeated_calls_are_identical(name, calls):
+    cfg = W.CONFIGS[name]
+    inp = W.make(cfg)
+    E, R = cfg.num_experts, cfg.num_ranks
+    x = U.to_dev_bf16(inp["x"])
+    idx = torch.from_numpy(inp["topk_idx"]).to(U.dev())
+    w = torch.from_numpy(inp["topk_weights"]).to(U.dev())
+    dtype = "fp8" if cfg.fp8 else "bf16"
+    lay = ep.ep_get_layout(idx, E, R)
+    d = ep.ep_dispatch(x, idx, w, lay, dtype=dtype)
+    y = U.to_dev_bf16(W.expert_output(d.recv_x.shape[0], cfg.hidden)) if cfg.fp8 else d.recv_x
+    out = ep.ep_combine(y, lay, idx, w)
+    torch.cuda.synchronize()
+    first = {"slot": lay.token_slot.clone(), "src": d.recv_src_idx.clone(),
+             "x": d.recv_x.view(torch.uint8).clone(), "out": out.clone()}
+    N = lay.num_recv()
+    # reference: the oracle
+    lay_o = oracle.get_layout(inp["topk_idx"], E, R)
+    assert np.array_equal(U.bits(lay.token_slot), lay_o["token_slot"])
+    for _ in range(calls):
+        ep.ep_get_layout(idx, E, R, layout=lay)
+        ep.ep_dispatch(x, idx, w, lay, dtype=dtype, out=d)
+        if not cfg.fp8:
+            y = d.recv_x
+        ep.ep_combine(y, lay, idx, w, out=out)
+    torch.cuda.synchronize()
+    assert lay.errors() == 0
+    assert torch.equal(lay.token_slot, first["slot"])
+    assert torch.equal(d.recv_src_idx[:N], first["src"][:N])
+    assert torch.equal(d.recv_x.view(torch.uint8)[:N], first["x"][:N])
+    assert torch.equal(out, first["out"])
+    # no duplicate (rank, source token) pair among the received rows
+    src = U.bits(d.recv_src_idx)[:N].astype(np.int64)
+    rank = np.searchsorted(U.bits(lay.rank_prefix), np.arange(N), side="right") - 1
+    pairs = rank * cfg.num_tokens + src
+    assert np.unique(pairs).size == N
