@@ -1,0 +1,82 @@
+"""Host-side logic of bench.py, CPU only: algorithmic byte counts, the
+ncu-traffic lookup, and the multi-replica aggregation (maximum over ranks,
+barriers) with two gloo ranks on 127.0.0.1."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import workloads as W  # noqa: E402
+
+
+def test_algorithmic_bytes_headline():
+    cfg = W.CONFIGS["fp8_8192x7168_top8_256e"]
+    b = bench.algorithmic_bytes(cfg, N=43409)
+    T, H, K, R = 8192, 7168, 8, 8
+    assert b["combine"] == 43409 * H * 2 + T * H * 2 + T * R * 4 + T * K * 12
+    assert abs(b["dispatch"] / 1e6 - 442) < 2
+    assert abs(b["combine"] / 1e6 - 741) < 2
+    bf = bench.algorithmic_bytes(W.CONFIGS["bf16_4096x4096_top6_64e"], N=18477)
+    assert bf["dispatch"] > 4096 * 4096 * 2 + 18477 * 4096 * 2
+
+
+def test_traffic_lookup_needs_matching_source(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    h = bench.kernel_source_hash("combine")
+    (prof / "ncu_dram_traffic.txt").write_text(
+        f"kernel=combine_kernel workload=w1 dram_bytes_per_launch=123 source_sha256={h}\n"
+        f"kernel=dispatch_kernel workload=w1 dram_bytes_per_launch=7 source_sha256=stale\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    # kernel_source_hash reads the sources under ROOT: point it back
+    monkeypatch.setattr(bench, "kernel_source_hash",
+                        lambda k, _h=bench.kernel_source_hash: {"combine": h}.get(k, "x"))
+    assert bench.ncu_traffic("combine", "w1") == 123
+    assert bench.ncu_traffic("dispatch", "w1") is None       # stale source
+    assert bench.ncu_traffic("combine", "other") is None
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world),
+                      RANK=str(rank), LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    bench.barrier(world)
+    mx = bench.max_over_ranks(1.5 + rank * 2.0, world)
+    bench.barrier(world)
+    q.put((rank, mx))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = dict(q.get(timeout=10) for _ in range(2))
+    assert res == {0: 3.5, 1: 3.5}
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    class A:
+        workload = W.HEADLINE
+        steps = 1
+        warmup = 3
+    assert bench.run_reference(A, rank=1, world=2) == 0

@@ -80,7 +80,7 @@ def test_large_workload_sampled():
     assert N <= cap
     rng = np.random.default_rng(5)
     toks = np.sort(rng.choice(cfg.num_tokens, size=1500, replace=False))
-    toks = np.concatenate([toks, [0, cfg.num_tokens - 1]])
+    toks = np.unique(np.concatenate([toks, [0, cfg.num_tokens - 1]]))
     local, glob = U.subset_problem(toks, lay_o["token_slot"])
     d_o = oracle.dispatch(inp["x"][toks], inp["topk_idx"][toks], inp["topk_weights"][toks],
                           E, R, local, True, len(glob))
