@@ -25,7 +25,8 @@ from ._native import (EP_ERRBIT_BAD_INDEX, EP_ERRBIT_CAPACITY,  # noqa: F401
                       EP_ERRBIT_TIMEOUT, EP_FP8_GROUP)
 
 __all__ = ["EPError", "Layout", "Dispatched", "ep_layout_workspace_bytes",
-           "ep_get_layout", "ep_dispatch", "ep_combine", "library_path"]
+           "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch", "ep_combine",
+           "library_path"]
 
 
 class EPError(RuntimeError):
@@ -129,6 +130,24 @@ def ep_get_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int,
     _check(N.load().ep_get_layout(
         _ptr(topk_idx), T, K, num_experts, num_ranks, C.byref(st),
         _ptr(layout.workspace), layout.workspace.numel(), _stream(stream, dev)), "ep_get_layout")
+    return layout
+
+
+def ep_get_layout_noalloc(topk_idx: torch.Tensor, num_experts: int, num_ranks: int,
+                          layout: Layout, stream=None) -> Layout:
+    """ep_get_layout without a workspace: for callers that cannot allocate
+    device memory when they call it.  The library's static scratch is used
+    instead (``layout.workspace`` is ignored); the first call on a device
+    should come before any stream capture, and calls must not overlap on
+    the GPU."""
+    _want(topk_idx, "topk_idx", torch.int64)
+    T, K = topk_idx.shape
+    if (layout.num_tokens, layout.num_experts, layout.num_ranks) != (T, num_experts, num_ranks):
+        raise ValueError("layout was allocated for other sizes")
+    st = layout.c_struct()
+    _check(N.load().ep_get_layout_noalloc(
+        _ptr(topk_idx), T, K, num_experts, num_ranks, C.byref(st),
+        _stream(stream, topk_idx.device)), "ep_get_layout_noalloc")
     return layout
 
 

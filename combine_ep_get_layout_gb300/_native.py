@@ -29,6 +29,7 @@ EP_MAX_TOPK = 32
 EP_MAX_EXPERTS = 4096
 EP_MAX_HIDDEN = 16384
 EP_FP8_GROUP = 128
+EP_NOALLOC_SCRATCH_BYTES = 256 * 1024
 
 
 class ep_layout_t(C.Structure):
@@ -48,6 +49,7 @@ _LP = C.POINTER(ep_layout_t)
 SIGNATURES = {
     "ep_layout_workspace_bytes": (_sz, [_i, _i, _i]),
     "ep_get_layout": (_i, [_p, _i, _i, _i, _i, _LP, _p, _sz, _p]),
+    "ep_get_layout_noalloc": (_i, [_p, _i, _i, _i, _i, _LP, _p]),
     "ep_dispatch": (_i, [_p, _i, _i, _p, _p, _i, _i, _i, _LP, _i, _p, _p, _p, _p, _p, _i, _p]),
     "ep_combine": (_i, [_p, _i, _i, _LP, _i, _i, _p, _p, _i, _i, _p, _p]),
     "ep_status_str": (C.c_char_p, [_i]),

@@ -134,6 +134,39 @@ ep_status_t ep_get_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
                           size_t workspace_bytes, ep_stream_t stream);
 
 /*
+ * ep_get_layout_noalloc: ep_get_layout for callers that cannot allocate
+ * device memory.  The pages have no counterpart to it; it is an interface
+ * addition of this library.
+ *
+ * Some callers have no way to obtain a workspace at call time: a plugin
+ * running inside another runtime's enqueue callback (an inference engine
+ * that owns all device memory and forbids new allocations once it is built),
+ * or a latency-critical serving loop where a cudaMalloc or cudaFree could
+ * synchronise the device and stall every other stream.  This entry point
+ * takes no workspace: its scratch (the layout kernel's barrier words and
+ * per-block rank totals) is a file-scope static device array of
+ * EP_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
+ * the library holds until the process exits.  It calls no allocating
+ * routine.  The caller still passes topk_idx and the layout outputs.
+ *
+ *   Limit: ep_layout_workspace_bytes(T, E, R) must not exceed
+ *   EP_NOALLOC_SCRATCH_BYTES, else EP_ERR_UNSUPPORTED (for R = 8 that is
+ *   T <= 2,095,104 tokens; for R = 64, T <= 261,888).
+ *   Set-up: the first call on a device looks up the device address of the
+ *   scratch array once (with that device current); make that first call
+ *   before any stream capture.
+ *   Every call clears the scratch it uses, on `stream`, before its kernel.
+ *   One scratch per device is shared by every call: calls that overlap on
+ *   the GPU (unordered streams) race on it and produce wrong layouts, so
+ *   order them (one stream, or events).
+ *   Arguments, outputs and errors are otherwise those of ep_get_layout.
+ */
+#define EP_NOALLOC_SCRATCH_BYTES (256u * 1024u)
+ep_status_t ep_get_layout_noalloc(const int64_t *topk_idx, int num_tokens, int num_topk,
+                                  int num_experts, int num_ranks,
+                                  const ep_layout_t *layout, ep_stream_t stream);
+
+/*
  * Dispatch: the scatter phase of TileScale PR #68 (PR summary: rows go
  * straight to their final compact index, no copy epilogue), with the fp8
  * cast of DeepEP's per_token_cast_to_fp8 layout fused into the same pass
