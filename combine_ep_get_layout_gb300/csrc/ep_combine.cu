@@ -4,7 +4,10 @@
 // comm_x[rank][src_token] is the received row token_slot[t][r] itself, so the
 // kernel gathers straight from the expert stage's output y.
 //
-// A CTA takes tokens t = blockIdx.x + i * gridDim.x.  Warp 0 compacts the
+// Two kernels: combine_ws_kernel (below, R <= 8) and combine_kernel, the
+// register kernel, used for more ranks.
+//
+// combine_kernel: a CTA takes tokens t = blockIdx.x + i * gridDim.x.  Warp 0 compacts the
 // token's valid (rank, slot) pairs in ascending rank order into shared memory
 // together with the rank's coefficient (1, or the fp32 sum in k order of the
 // token's gate weights on that rank).  Then every thread owns 16-byte columns
@@ -12,6 +15,7 @@
 // accumulates them, in ascending rank order, in fp32 with separate multiply
 // and add, and stores the bf16 result rounded to nearest even.
 #include <algorithm>
+#include <mutex>
 
 #include "ep_device.cuh"
 
@@ -20,6 +24,7 @@ namespace {
 
 constexpr int kCombineThreads = 128;
 constexpr int kRowsPerBatch = 8;
+constexpr int kCombineCols = 1;  // 16-byte columns per thread per pass
 
 struct CombineParams {
   const uint16_t *y;
@@ -59,6 +64,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
   const int warp = tid / kWarpSize;
   const int ncol = p.H / 8;  // 16-byte columns
   const uint32_t lanes_below = (1u << lane) - 1u;
+  griddep_wait();
+  griddep_launch_dependents();
 
   int i = 0;
   for (int t = blockIdx.x; t < p.T; t += gridDim.x, ++i) {
@@ -98,29 +105,247 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
 
     const int n = s_n[b];
     uint16_t *out_row = p.out + (size_t)t * p.H;
-    for (int col = tid; col < ncol; col += kCombineThreads) {
-      float acc[8];
+    for (int col0 = tid; col0 < ncol; col0 += kCombineThreads * kCombineCols) {
+      float acc[kCombineCols][8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+      for (int c = 0; c < kCombineCols; ++c)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[c][q] = 0.0f;
       for (int j0 = 0; j0 < n; j0 += kRowsPerBatch) {
-        int4 v[kRowsPerBatch];
+        int4 v[kCombineCols][kRowsPerBatch];
 #pragma unroll
-        for (int q = 0; q < kRowsPerBatch; ++q)
-          if (j0 + q < n) v[q] = ld_stream_v4(p.y + (size_t)s_slot[b][j0 + q] * p.H + (size_t)col * 8);
+        for (int c = 0; c < kCombineCols; ++c) {
+          const int col = col0 + c * kCombineThreads;
 #pragma unroll
-        for (int q = 0; q < kRowsPerBatch; ++q)
-          if (j0 + q < n) accumulate<WEIGHTED>(acc, v[q], s_coef[b][j0 + q]);
+          for (int q = 0; q < kRowsPerBatch; ++q)
+            if (j0 + q < n && col < ncol)
+              v[c][q] = ld_stream_v4(p.y + (size_t)s_slot[b][j0 + q] * p.H + (size_t)col * 8);
+        }
+#pragma unroll
+        for (int c = 0; c < kCombineCols; ++c)
+#pragma unroll
+          for (int q = 0; q < kRowsPerBatch; ++q)
+            if (j0 + q < n) accumulate<WEIGHTED>(acc[c], v[c][q], s_coef[b][j0 + q]);
       }
-      int4 o;
-      o.x = (int)pack_bf16x2(acc[0], acc[1]);
-      o.y = (int)pack_bf16x2(acc[2], acc[3]);
-      o.z = (int)pack_bf16x2(acc[4], acc[5]);
-      o.w = (int)pack_bf16x2(acc[6], acc[7]);
-      st_stream_v4(out_row + (size_t)col * 8, o);
+#pragma unroll
+      for (int c = 0; c < kCombineCols; ++c) {
+        const int col = col0 + c * kCombineThreads;
+        if (col >= ncol) continue;
+        int4 o;
+        o.x = (int)pack_bf16x2(acc[c][0], acc[c][1]);
+        o.y = (int)pack_bf16x2(acc[c][2], acc[c][3]);
+        o.z = (int)pack_bf16x2(acc[c][4], acc[c][5]);
+        o.w = (int)pack_bf16x2(acc[c][6], acc[c][7]);
+        st_stream_v4(out_row + (size_t)col * 8, o);
+      }
     }
     // s_slot[b] is rewritten two tokens later, after the next barrier.
   }
 }
+
+// ------------------------------------------------------------------------
+// Warp-specialised kernel (R <= kWsMaxRanks).  A unit is one token's
+// kChunk-element slice of the row; a CTA takes tokens
+// t = blockIdx.x + j * gridDim.x and all units of a token in a row.
+//   warp 0 (loader)   fetches a token's slots, expert ids and weights one
+//                     token ahead (lanes in parallel), forms each rank's
+//                     coefficient by shuffles, compacts the valid ranks in
+//                     ascending order into each unit's stage header and
+//                     issues one bulk (TMA 1D) load per valid row slice into
+//                     the stage (one mbarrier, expected bytes = rows x slice);
+//   warps 1.. (reducers) sum the stage's rows in rank order, one 16-byte
+//                     column per thread (fp32, separate multiply and add),
+//                     store the bf16 result and release the stage.
+// The loader runs `stages` units ahead, so the memory pipe does not wait on
+// the per-token metadata or on the reduction.
+
+constexpr int kWsMaxRanks = 8;
+constexpr int kChunk = 2048;                   // elements per unit
+constexpr int kChunkBytes = kChunk * 2;
+constexpr int kReducers = 8;                   // warps
+constexpr int kWsCombineThreads = (1 + kReducers) * kWarpSize;
+constexpr int kCombineStages = 2;
+constexpr int kStageHeader = 128;              // n, coefficients
+constexpr int kStageBytes = kStageHeader + kWsMaxRanks * kChunkBytes;
+
+// One token's routing as the loader warp holds it: lane r < R has the slot
+// of rank r, lane k < K the k-th expert id and gate weight.
+struct TokenMeta {
+  int slot;
+  int64_t e;
+  float w;
+};
+
+__device__ __forceinline__ TokenMeta fetch_meta(const CombineParams &p, int t, int lane, bool weighted) {
+  TokenMeta m;
+  m.slot = lane < p.R ? __ldg(p.token_slot + (size_t)t * p.R + lane) : -1;
+  m.e = (weighted && lane < p.K) ? __ldg(p.topk_idx + (size_t)t * p.K + lane) : -1;
+  m.w = (weighted && lane < p.K) ? __ldg(p.topk_weights + (size_t)t * p.K + lane) : 0.0f;
+  return m;
+}
+
+template <bool WEIGHTED>
+__global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombineParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [kCombineStages]
+  uint64_t *empty = full + kCombineStages;              // [kCombineStages]
+  volatile int *s_abort = reinterpret_cast<volatile int *>(smem + 64);
+  unsigned char *stages = smem + 128;
+
+  const int tid = threadIdx.x;
+  const int warp = tid / kWarpSize;
+  const int lane = tid & (kWarpSize - 1);
+  const int nchunk = (p.H + kChunk - 1) / kChunk;
+  // a CTA takes tokens t = blockIdx.x + j * gridDim.x, all chunks of a token in a row
+  const int ntok = p.T > (int)blockIdx.x ? (p.T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+
+  if (tid == 0) {
+    for (int s = 0; s < kCombineStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kReducers);
+    }
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();
+
+  const uint32_t lanes_below = (1u << lane) - 1u;
+  long loads_issued = 0;  // loader lane 0 only
+  if (warp == 0) {
+    long i = 0;  // unit counter: stage i % kCombineStages
+    TokenMeta cur = ntok > 0 ? fetch_meta(p, blockIdx.x, lane, WEIGHTED) : TokenMeta{-1, -1, 0.0f};
+    for (int j = 0; j < ntok && !*s_abort; ++j) {
+      const int t = blockIdx.x + j * gridDim.x;
+      TokenMeta nxt = cur;
+      if (j + 1 < ntok) nxt = fetch_meta(p, t + gridDim.x, lane, WEIGHTED);  // in flight meanwhile
+      int slot = cur.slot;
+      if (slot >= p.cap) {
+        set_error(p.error_word, EP_ERRBIT_CAPACITY);
+        slot = -1;
+      }
+      float coef = 1.0f;
+      if (WEIGHTED) {
+        // rank `lane`'s coefficient: the fp32 sum, in k order, of the weights
+        // of the token's experts on that rank
+        coef = 0.0f;
+        for (int k = 0; k < p.K; ++k) {
+          const int64_t e = __shfl_sync(0xffffffffu, cur.e, k);
+          const float w = __shfl_sync(0xffffffffu, cur.w, k);
+          if (e >= 0 && e < p.E && static_cast<int>(e) / p.epr == lane) coef = __fadd_rn(coef, w);
+        }
+      }
+      const uint32_t bal = __ballot_sync(0xffffffffu, slot >= 0);
+      const int nrows = __popc(bal);
+      const int pos = __popc(bal & lanes_below);
+      for (int c = 0; c < nchunk; ++c, ++i) {
+        const int s = static_cast<int>(i % kCombineStages);
+        const int elems = min(kChunk, p.H - c * kChunk);
+        unsigned char *stage = stages + (size_t)s * kStageBytes;
+        if (i >= kCombineStages) {
+          const bool ok = __all_sync(0xffffffffu,
+                                     mbar_wait_bounded(&empty[s], (uint32_t)(i / kCombineStages - 1) & 1u));
+          if (!ok) {
+            if (lane == 0) {
+              *s_abort = 1;
+              set_error(p.error_word, EP_ERRBIT_TIMEOUT);
+            }
+            break;
+          }
+        }
+        float *hdr_coef = reinterpret_cast<float *>(stage + 16);
+        if (slot >= 0) hdr_coef[pos] = coef;
+        if (lane == 0) *reinterpret_cast<int *>(stage) = nrows;
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)nrows * (uint32_t)elems * 2u);
+        __syncwarp();
+        if (slot >= 0)
+          bulk_load(stage + kStageHeader + (size_t)pos * kChunkBytes,
+                    p.y + (size_t)slot * p.H + (size_t)c * kChunk, (uint32_t)elems * 2u, &full[s]);
+        if (lane == 0) loads_issued = i + 1;
+      }
+      cur = nxt;
+    }
+  } else {
+    const int rt = tid - kWarpSize;  // reducer thread
+    long i = 0;
+    for (int j = 0; j < ntok && !*s_abort; ++j) {
+      const int t = blockIdx.x + j * gridDim.x;
+      bool ok = true;
+      for (int c = 0; c < nchunk; ++c, ++i) {
+        const int s = static_cast<int>(i % kCombineStages);
+        const int cols = min(kChunk, p.H - c * kChunk) / 8;
+        const unsigned char *stage = stages + (size_t)s * kStageBytes;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (uint32_t)(i / kCombineStages) & 1u))) {
+          if (lane == 0) {
+            *s_abort = 1;
+            set_error(p.error_word, EP_ERRBIT_TIMEOUT);
+          }
+          ok = false;
+          break;
+        }
+        const int nrows = *reinterpret_cast<const int *>(stage);
+        const float *hdr_coef = reinterpret_cast<const float *>(stage + 16);
+        uint16_t *out = p.out + (size_t)t * p.H + (size_t)c * kChunk;
+        for (int col = rt; col < cols; col += kReducers * kWarpSize) {
+          float acc[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+          for (int r = 0; r < nrows; ++r) {
+            const int4 v =
+                *reinterpret_cast<const int4 *>(stage + kStageHeader + (size_t)r * kChunkBytes + col * 16);
+            accumulate<WEIGHTED>(acc, v, hdr_coef[r]);
+          }
+          int4 o;
+          o.x = (int)pack_bf16x2(acc[0], acc[1]);
+          o.y = (int)pack_bf16x2(acc[2], acc[3]);
+          o.z = (int)pack_bf16x2(acc[4], acc[5]);
+          o.w = (int)pack_bf16x2(acc[6], acc[7]);
+          st_stream_v4(out + (size_t)col * 8, o);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      }
+      if (!ok) break;
+    }
+  }
+
+  // After an abort, the loads of the latest units still in flight are
+  // waited for (bounded) before the CTA's shared memory is released.
+  __syncthreads();
+  if (*s_abort && tid == 0) {
+    for (long m = loads_issued > kCombineStages ? loads_issued - kCombineStages : 0; m < loads_issued; ++m)
+      (void)mbar_wait_bounded(&full[m % kCombineStages], (uint32_t)(m / kCombineStages) & 1u);
+  }
+}
+
+template <bool WEIGHTED>
+ep_status_t launch_ws(const CombineParams &p, const DeviceInfo &di, cudaStream_t stream) {
+  static std::mutex mu;
+  static bool configured[64] = {};
+  const size_t smem = 128 + (size_t)kCombineStages * kStageBytes;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (di.device < 64 && !configured[di.device]) {
+      cudaError_t e = cudaFuncSetAttribute(combine_ws_kernel<WEIGHTED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(combine_ws_kernel)");
+      configured[di.device] = true;
+    }
+  }
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_ws_kernel<WEIGHTED>,
+                                                                kWsCombineThreads, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(combine_ws)");
+  if (per_sm <= 0) return fail(EP_ERR_UNSUPPORTED, "ep_combine: kernel cannot be resident");
+  const int grid = std::min(p.T, per_sm * di.num_sms);
+  e = launch_kernel(combine_ws_kernel<WEIGHTED>, grid, kWsCombineThreads, smem, stream, false, p);
+  if (e != cudaSuccess) return cuda_fail(e, "launch combine_ws_kernel");
+  return EP_OK;
+}
+
+constexpr bool kUseWsCombine = true;
 
 template <bool WEIGHTED>
 ep_status_t launch_impl(const CombineParams &p, const DeviceInfo &di, cudaStream_t stream) {
@@ -130,8 +355,7 @@ ep_status_t launch_impl(const CombineParams &p, const DeviceInfo &di, cudaStream
   if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(combine)");
   if (per_sm <= 0) return fail(EP_ERR_UNSUPPORTED, "ep_combine: kernel cannot be resident");
   const int grid = std::min(p.T, per_sm * di.num_sms);
-  combine_kernel<WEIGHTED><<<grid, kCombineThreads, 0, stream>>>(p);
-  e = cudaGetLastError();
+  e = launch_kernel(combine_kernel<WEIGHTED>, grid, kCombineThreads, 0, stream, false, p);
   if (e != cudaSuccess) return cuda_fail(e, "launch combine_kernel");
   return EP_OK;
 }
@@ -156,7 +380,10 @@ ep_status_t launch_combine(const CombineArgs &a, cudaStream_t stream) {
   p.topk_idx = a.topk_idx;
   p.topk_weights = a.topk_weights;
   p.out = a.out;
-  return a.topk_weights != nullptr ? launch_impl<true>(p, *di, stream) : launch_impl<false>(p, *di, stream);
+  const bool weighted = a.topk_weights != nullptr;
+  if (kUseWsCombine && a.num_ranks <= kWsMaxRanks)
+    return weighted ? launch_ws<true>(p, *di, stream) : launch_ws<false>(p, *di, stream);
+  return weighted ? launch_impl<true>(p, *di, stream) : launch_impl<false>(p, *di, stream);
 }
 
 }  // namespace ep

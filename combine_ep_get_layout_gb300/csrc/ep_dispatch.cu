@@ -4,8 +4,9 @@
 // cast fused into the same pass (same page, commit message on packing the
 // fp8 row; DeepEP's per_token_cast_to_fp8 layout).
 //
-// One CTA works through its tokens (t = blockIdx.x + i * gridDim.x) with a
-// ring of `stages` shared-memory row buffers:
+// dispatch_ring_kernel: one CTA works through its tokens
+// (t = blockIdx.x + i * gridDim.x) with a ring of `stages` shared-memory row
+// buffers:
 //   - a bulk (TMA 1D) copy brings token i's bf16 row into its stage, signalled
 //     on an mbarrier; loads run `stages - 1` tokens ahead;
 //   - bf16: warp 0 issues one bulk store of the stage per destination rank,
@@ -29,6 +30,9 @@ constexpr int kDispatchWarps = kDispatchThreads / kWarpSize;
 constexpr int kMaxStages = 8;
 constexpr int kHeaderBytes = 1024;  // mbarriers, flags, slot buffers
 constexpr size_t kSmemBudget = 80 * 1024;  // per CTA: aims at >= 2-3 CTAs per SM
+constexpr int kWsStages = 2;                 // bf16 row stages of the fp8 kernel
+constexpr size_t kWsSmemBudget = 64 * 1024;
+constexpr bool kFp8WarpSpecialised = true;
 
 struct DispatchParams {
   const uint16_t *x;
@@ -101,8 +105,29 @@ __device__ __forceinline__ void write_metadata(const DispatchParams &p, int t,
   }
 }
 
+// The fp8 cast of one 128-element group held by a warp, four bf16 values per
+// lane (`raw`, in element order): amax over the group by shuffles,
+// scale = amax / 448 and code = e4m3(x / scale) with IEEE division, round to
+// nearest even, saturating at +-448.  An all-zero group has scale 0 and keeps
+// each zero's sign.  Returns the lane's four codes (element order, low byte
+// first); `scale` receives the group's scale in every lane.
+__device__ __forceinline__ uint32_t cast_group(uint2 raw, float &scale) {
+  const float v0 = bf16_lo(raw.x), v1 = bf16_hi(raw.x);
+  const float v2 = bf16_lo(raw.y), v3 = bf16_hi(raw.y);
+  float a = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+  scale = __fdiv_rn(a, 448.0f);
+  const bool nz = a > 0.0f;
+  const float u0 = nz ? __fdiv_rn(v0, scale) : v0;
+  const float u1 = nz ? __fdiv_rn(v1, scale) : v1;
+  const float u2 = nz ? __fdiv_rn(v2, scale) : v2;
+  const float u3 = nz ? __fdiv_rn(v3, scale) : v3;
+  return pack_e4m3x2(u0, u1) | (pack_e4m3x2(u2, u3) << 16);
+}
+
 template <bool FP8>
-__global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchParams p) {
+__global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(DispatchParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);               // [kMaxStages]
   int *s_abort = reinterpret_cast<int *>(smem + 64);
@@ -123,6 +148,8 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchPara
     fence_barrier_init();
   }
   __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();
   const uint64_t policy = policy_evict_first();  // x is read exactly once
   int loads_issued = 0;                           // meaningful in thread 0 only
   if (tid == 0)
@@ -153,20 +180,9 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchPara
       unsigned char *orow = obuf + (size_t)b * p.out_stride;
       float *srow = sbuf + (size_t)b * (p.scale_stride / 4);
       for (int g = warp; g < p.groups; g += kDispatchWarps) {
+        float scale;
         const uint2 raw = *reinterpret_cast<const uint2 *>(stage + (size_t)g * 256 + lane * 8);
-        const float v0 = bf16_lo(raw.x), v1 = bf16_hi(raw.x);
-        const float v2 = bf16_lo(raw.y), v3 = bf16_hi(raw.y);
-        float a = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-        const float scale = __fdiv_rn(a, 448.0f);
-        const bool nz = a > 0.0f;  // an all-zero group keeps each zero's sign
-        const float u0 = nz ? __fdiv_rn(v0, scale) : v0;
-        const float u1 = nz ? __fdiv_rn(v1, scale) : v1;
-        const float u2 = nz ? __fdiv_rn(v2, scale) : v2;
-        const float u3 = nz ? __fdiv_rn(v3, scale) : v3;
-        *reinterpret_cast<uint32_t *>(orow + (size_t)g * 128 + lane * 4) =
-            pack_e4m3x2(u0, u1) | (pack_e4m3x2(u2, u3) << 16);
+        *reinterpret_cast<uint32_t *>(orow + (size_t)g * 128 + lane * 4) = cast_group(raw, scale);
         if (lane == 0) srow[g] = scale;
       }
       fence_proxy_async_smem();
@@ -226,6 +242,221 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchPara
   }
 }
 
+
+
+// ------------------------------------------------------------------------
+// Warp-specialised fp8 kernel.  Roles inside one CTA, handing buffers over
+// through mbarriers (no CTA-wide barrier in the loop):
+//   warp 0 (loader)    bulk-loads token rows into a ring of `stages` bf16
+//                      row buffers (full_in), reusing a buffer once every
+//                      caster has released it (empty_in);
+//   warp 1 (storer)    writes the received metadata, then bulk-stores each
+//                      cast row and its scales to every destination slot
+//                      (full_out), releasing the buffer once the stores have
+//                      read it (empty_out);
+//   warps 2.. (casters) cast 128-element groups of a row into one of two
+//                      fp8 row buffers.
+// Casting token i+1 thus overlaps the stores of token i and the loads of
+// the tokens after it.
+
+constexpr int kWsCasters = 8;
+constexpr int kWsThreads = (2 + kWsCasters) * kWarpSize;
+constexpr int kWsOut = 2;
+
+__global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int S = p.stages;
+  uint64_t *full_in = reinterpret_cast<uint64_t *>(smem);  // [S]
+  uint64_t *empty_in = full_in + kMaxStages;                // [S]
+  uint64_t *full_out = empty_in + kMaxStages;               // [kWsOut]
+  uint64_t *empty_out = full_out + kWsOut;                  // [kWsOut]
+  volatile int *s_abort = reinterpret_cast<volatile int *>(smem + 256);
+  int32_t *s_slot = reinterpret_cast<int32_t *>(smem + 512);  // [EP_MAX_RANKS], storer only
+  unsigned char *in = smem + kHeaderBytes;
+  unsigned char *out = in + (size_t)S * p.stage_stride;
+  float *osc = reinterpret_cast<float *>(out + (size_t)kWsOut * p.out_stride);
+
+  const int tid = threadIdx.x;
+  const int warp = tid / kWarpSize;
+  const int lane = tid & (kWarpSize - 1);
+  const int n = (p.T > (int)blockIdx.x) ? (p.T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full_in[s], 1);
+      mbar_init(&empty_in[s], kWsCasters);
+    }
+    for (int o = 0; o < kWsOut; ++o) {
+      mbar_init(&full_out[o], kWsCasters);
+      mbar_init(&empty_out[o], 1);
+    }
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();
+
+  int loads_issued = 0;  // loader lane 0 only
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t policy = policy_evict_first();
+      for (int i = 0; i < n && !*s_abort; ++i) {
+        const int s = i % S;
+        if (i >= S && !mbar_wait_bounded(&empty_in[s], (uint32_t)(i / S - 1) & 1u)) {
+          *s_abort = 1;
+          set_error(p.error_word, EP_ERRBIT_TIMEOUT);
+          break;
+        }
+        const int t = blockIdx.x + i * gridDim.x;
+        mbar_arrive_expect_tx(&full_in[s], p.row_in_bytes);
+        bulk_load_hint(in + (size_t)s * p.stage_stride, p.x + (size_t)t * p.H, p.row_in_bytes, &full_in[s],
+                       policy);
+        loads_issued = i + 1;
+      }
+    }
+  } else if (warp == 1) {
+    const bool scale_bulk = p.scale_stride == (uint32_t)p.groups * 4u &&
+                            (reinterpret_cast<uintptr_t>(p.recv_x_scales) & 15u) == 0;
+    for (int i = 0; i < n && !*s_abort; ++i) {
+      const int t = blockIdx.x + i * gridDim.x;
+      const int o = i % kWsOut;
+      const int32_t *srow = p.token_slot + (size_t)t * p.R;
+      int slot_lo = lane < p.R ? __ldg(srow + lane) : -1;
+      int slot_hi = lane + kWarpSize < p.R ? __ldg(srow + lane + kWarpSize) : -1;
+      if (slot_lo >= p.cap) {
+        set_error(p.error_word, EP_ERRBIT_CAPACITY);
+        slot_lo = -1;
+      }
+      if (slot_hi >= p.cap) {
+        set_error(p.error_word, EP_ERRBIT_CAPACITY);
+        slot_hi = -1;
+      }
+      const int64_t e = lane < p.K ? __ldg(p.topk_idx + (size_t)t * p.K + lane) : -1;
+      const float w = (lane < p.K && p.recv_topk_weights != nullptr)
+                          ? __ldg(p.topk_weights + (size_t)t * p.K + lane) : 0.0f;
+      // received metadata: needs no shared memory, runs ahead of the cast
+      for (int r = 0; r < p.R; ++r) {
+        const int slot = __shfl_sync(0xffffffffu, r < kWarpSize ? slot_lo : slot_hi, r & (kWarpSize - 1));
+        if (slot < 0) continue;
+        if (lane == 0 && p.recv_src_idx != nullptr) p.recv_src_idx[slot] = t;
+        if (lane < p.K) {
+          const bool here = e >= 0 && e < p.E && static_cast<int>(e) / p.epr == r;
+          if (p.recv_topk_idx != nullptr)
+            p.recv_topk_idx[(size_t)slot * p.K + lane] = here ? static_cast<int>(e) - r * p.epr : -1;
+          if (p.recv_topk_weights != nullptr) p.recv_topk_weights[(size_t)slot * p.K + lane] = here ? w : 0.0f;
+        }
+      }
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full_out[o], (uint32_t)(i / kWsOut) & 1u));
+      if (!ok) {
+        if (lane == 0) {
+          *s_abort = 1;
+          set_error(p.error_word, EP_ERRBIT_TIMEOUT);
+        }
+        break;
+      }
+      const unsigned char *orow = out + (size_t)o * p.out_stride;
+      const float *oscale = osc + (size_t)o * (p.scale_stride / 4);
+      if (slot_lo >= 0) {
+        bulk_store(static_cast<unsigned char *>(p.recv_x) + (size_t)slot_lo * p.H, orow, p.row_out_bytes);
+        if (scale_bulk) bulk_store(p.recv_x_scales + (size_t)slot_lo * p.groups, oscale, p.scale_stride);
+      }
+      if (slot_hi >= 0) {
+        bulk_store(static_cast<unsigned char *>(p.recv_x) + (size_t)slot_hi * p.H, orow, p.row_out_bytes);
+        if (scale_bulk) bulk_store(p.recv_x_scales + (size_t)slot_hi * p.groups, oscale, p.scale_stride);
+      }
+      bulk_commit();
+      if (!scale_bulk) {
+        s_slot[lane] = slot_lo;
+        if (p.R > kWarpSize) s_slot[lane + kWarpSize] = slot_hi;
+        __syncwarp();
+        const int RG = p.R * p.groups;
+        for (int q = lane; q < RG; q += kWarpSize) {
+          const int r = q / p.groups;
+          const int g = q - r * p.groups;
+          const int slot = s_slot[r];
+          if (slot >= 0) p.recv_x_scales[(size_t)slot * p.groups + g] = oscale[g];
+        }
+      }
+      bulk_wait_read<0>();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_out[o]);
+    }
+    bulk_wait<0>();
+  } else {
+    const int cw = warp - 2;
+    for (int i = 0; i < n && !*s_abort; ++i) {
+      const int s = i % S;
+      const int o = i % kWsOut;
+      bool ok = mbar_wait_bounded(&full_in[s], (uint32_t)(i / S) & 1u);
+      if (ok && i >= kWsOut) ok = mbar_wait_bounded(&empty_out[o], (uint32_t)(i / kWsOut - 1) & 1u);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) {
+          *s_abort = 1;
+          set_error(p.error_word, EP_ERRBIT_TIMEOUT);
+        }
+        break;
+      }
+      const unsigned char *stage = in + (size_t)s * p.stage_stride;
+      unsigned char *orow = out + (size_t)o * p.out_stride;
+      float *oscale = osc + (size_t)o * (p.scale_stride / 4);
+      for (int g = cw; g < p.groups; g += kWsCasters) {
+        float scale;
+        const uint2 raw = *reinterpret_cast<const uint2 *>(stage + (size_t)g * 256 + lane * 8);
+        *reinterpret_cast<uint32_t *>(orow + (size_t)g * 128 + lane * 4) = cast_group(raw, scale);
+        if (lane == 0) oscale[g] = scale;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&empty_in[s]);
+        mbar_arrive(&full_out[o]);
+      }
+    }
+  }
+
+  // After an abort, loads still in flight are waited for (bounded) before
+  // the CTA's shared memory is released.  Only the latest load of each stage
+  // (the last S issued) can still be in flight.
+  __syncthreads();
+  if (*s_abort && tid == 0) {
+    for (int m = max(0, loads_issued - S); m < loads_issued; ++m)
+      (void)mbar_wait_bounded(&full_in[m % S], (uint32_t)(m / S) & 1u);
+  }
+}
+
+size_t ws_smem_bytes(const DispatchParams &p) {
+  return kHeaderBytes + (size_t)p.stages * p.stage_stride + kWsOut * ((size_t)p.out_stride + p.scale_stride);
+}
+
+ep_status_t launch_ws(DispatchParams &p, const DeviceInfo &di, cudaStream_t stream) {
+  static std::mutex mu;
+  static bool configured[64] = {};
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (di.device < 64 && !configured[di.device]) {
+      cudaError_t e = cudaFuncSetAttribute(dispatch_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)di.max_smem_per_block_optin);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(dispatch_ws_kernel)");
+      configured[di.device] = true;
+    }
+  }
+  p.stages = kWsStages;
+  while (p.stages > 2 && ws_smem_bytes(p) > kWsSmemBudget) --p.stages;
+  const size_t smem = ws_smem_bytes(p);
+  if (smem > di.max_smem_per_block_optin)
+    return fail(EP_ERR_UNSUPPORTED, "ep_dispatch: hidden %d needs %zu bytes of shared memory", p.H, smem);
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_ws_kernel, kWsThreads, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(dispatch_ws)");
+  if (per_sm <= 0) return fail(EP_ERR_UNSUPPORTED, "ep_dispatch: kernel cannot be resident");
+  const int grid = std::min(p.T, per_sm * di.num_sms);
+  e = launch_kernel(dispatch_ws_kernel, grid, kWsThreads, smem, stream, false, p);
+  if (e != cudaSuccess) return cuda_fail(e, "launch dispatch_ws_kernel");
+  return EP_OK;
+}
+
+
 size_t dispatch_smem_bytes(const DispatchParams &p, bool fp8) {
   size_t bytes = kHeaderBytes + (size_t)p.stages * p.stage_stride;
   if (fp8) bytes += 2 * (size_t)p.out_stride + 2 * (size_t)p.scale_stride;
@@ -233,15 +464,15 @@ size_t dispatch_smem_bytes(const DispatchParams &p, bool fp8) {
 }
 
 template <bool FP8>
-ep_status_t launch_impl(DispatchParams &p, const DeviceInfo &di, cudaStream_t stream) {
+ep_status_t launch_ring(DispatchParams &p, const DeviceInfo &di, cudaStream_t stream) {
   static std::mutex mu;
   static bool configured[64] = {};
   {
     std::lock_guard<std::mutex> g(mu);
     if (di.device < 64 && !configured[di.device]) {
-      cudaError_t e = cudaFuncSetAttribute(dispatch_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaError_t e = cudaFuncSetAttribute(dispatch_ring_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)di.max_smem_per_block_optin);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(dispatch_kernel)");
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(dispatch_ring_kernel)");
       configured[di.device] = true;
     }
   }
@@ -252,14 +483,13 @@ ep_status_t launch_impl(DispatchParams &p, const DeviceInfo &di, cudaStream_t st
   if (smem > di.max_smem_per_block_optin)
     return fail(EP_ERR_UNSUPPORTED, "ep_dispatch: hidden %d needs %zu bytes of shared memory", p.H, smem);
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_kernel<FP8>,
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_ring_kernel<FP8>,
                                                                 kDispatchThreads, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(dispatch)");
   if (per_sm <= 0) return fail(EP_ERR_UNSUPPORTED, "ep_dispatch: kernel cannot be resident");
   const int grid = std::min(p.T, per_sm * di.num_sms);
-  dispatch_kernel<FP8><<<grid, kDispatchThreads, smem, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "launch dispatch_kernel");
+  e = launch_kernel(dispatch_ring_kernel<FP8>, grid, kDispatchThreads, smem, stream, false, p);
+  if (e != cudaSuccess) return cuda_fail(e, "launch dispatch_ring_kernel");
   return EP_OK;
 }
 
@@ -293,7 +523,8 @@ ep_status_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream) {
   p.stage_stride = (p.row_in_bytes + 127u) / 128u * 128u;
   p.out_stride = a.fp8 ? ((uint32_t)a.hidden + 127u) / 128u * 128u : 0u;
   p.scale_stride = a.fp8 ? ((uint32_t)p.groups * 4u + 15u) / 16u * 16u : 0u;
-  return a.fp8 ? launch_impl<true>(p, *di, stream) : launch_impl<false>(p, *di, stream);
+  if (a.fp8) return kFp8WarpSpecialised ? launch_ws(p, *di, stream) : launch_ring<true>(p, *di, stream);
+  return launch_ring<false>(p, *di, stream);
 }
 
 }  // namespace ep

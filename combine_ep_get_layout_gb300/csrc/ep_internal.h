@@ -12,6 +12,11 @@ namespace ep {
 
 constexpr int kWarpSize = 32;
 
+// Kernels are launched with programmatic stream serialization: each may be
+// scheduled while the kernel ahead of it drains, and waits (griddep_wait)
+// before touching global memory.
+constexpr bool kUsePdl = true;
+
 // Properties of the current device, queried once per device.
 struct DeviceInfo {
   int device = -1;

@@ -25,7 +25,7 @@
 namespace ep {
 namespace {
 
-constexpr int kLayoutThreads = 256;
+constexpr int kLayoutThreads = 128;  // one token per thread per chunk
 constexpr int kLayoutWarps = kLayoutThreads / kWarpSize;
 constexpr size_t kPartialOffset = 256;  // bytes: barrier words come first
 
@@ -45,11 +45,14 @@ struct LayoutParams {
 
 size_t layout_smem_bytes(int tokens_per_block, int E, int R) {
   // masks[tpb] u64, hist[E], blk_cnt[R], warp_off[W*R], chunk_tot[R],
-  // tot[R], before[R], base[R+1], run[R], flags[2]
-  size_t ints = (size_t)E + R + (size_t)kLayoutWarps * R + R + R + R + (R + 1) + R + 2;
+  // tot[R], before[R], base[R+1], run[R], flags[2], scan_all[T], scan_before[T]
+  size_t ints = (size_t)E + R + (size_t)kLayoutWarps * R + R + R + R + (R + 1) + R + 2 + 2 * kLayoutThreads;
   return (size_t)tokens_per_block * sizeof(uint64_t) + ints * sizeof(int32_t);
 }
 
+// KMAX bounds the unrolled index loads: all K ids of a token are requested
+// before the first is used.
+template <int KMAX>
 __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x;
@@ -69,10 +72,14 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutParams p) 
   int *base = before + R;  // [R + 1]
   int *run = base + R + 1;
   int *flags = run + R;  // [0] bad index seen, [1] barrier timed out
+  int *scan_all = flags + 2;                  // [kLayoutThreads]
+  int *scan_before = scan_all + kLayoutThreads;  // [kLayoutThreads]
 
   for (int i = tid; i < E; i += kLayoutThreads) hist[i] = 0;
   for (int i = tid; i < R; i += kLayoutThreads) blk_cnt[i] = 0;
   if (tid < 2) flags[tid] = 0;
+  griddep_wait();
+  griddep_launch_dependents();
   if (b == 0) {
     // Cleared before the barrier; every block adds into them after it.
     for (int i = tid; i < E; i += kLayoutThreads) p.out.num_tokens_per_expert[i] = 0;
@@ -90,8 +97,12 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutParams p) 
     uint64_t mask = 0;
     if (t < end) {
       const int64_t *row = p.topk_idx + (size_t)t * K;
-      for (int k = 0; k < K; ++k) {
-        const int64_t e = __ldg(row + k);
+      int64_t ids[KMAX];
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) ids[k] = k < K ? __ldg(row + k) : -1;
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        const int64_t e = ids[k];
         if (e == -1) continue;
         if (e < 0 || e >= E) {
           bad = true;
@@ -129,13 +140,26 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutParams p) 
   }
   __syncthreads();
 
-  // ---- phase 2: bases (exclusive scan over ranks and over earlier blocks)
-  for (int r = tid; r < R; r += kLayoutThreads) {
+  // ---- phase 2: bases (exclusive scan over ranks and over earlier blocks);
+  // the block totals are summed by kLayoutThreads / R threads per rank
+  const int per_rank = kLayoutThreads / R;  // >= 2 since R <= 64
+  if (tid < per_rank * R) {
+    const int r = tid % R;
     int all = 0, earlier = 0;
-    for (int bb = 0; bb < G; ++bb) {
+    for (int bb = tid / R; bb < G; bb += per_rank) {
       const int v = __ldcg(&p.partial[(size_t)bb * R + r]);
       all += v;
       if (bb < b) earlier += v;
+    }
+    scan_all[tid] = all;
+    scan_before[tid] = earlier;
+  }
+  __syncthreads();
+  for (int r = tid; r < R; r += kLayoutThreads) {
+    int all = 0, earlier = 0;
+    for (int q = 0; q < per_rank; ++q) {
+      all += scan_all[q * R + r];
+      earlier += scan_before[q * R + r];
     }
     tot[r] = all;
     before[r] = earlier;
@@ -247,14 +271,17 @@ ep_status_t launch_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
   const DeviceInfo *di = current_device_info();
   if (di == nullptr) return EP_ERR_CUDA;
 
+  const auto kernel = num_topk <= 8 ? layout_kernel<8> : layout_kernel<EP_MAX_TOPK>;
   static std::mutex mu;
   static bool configured[64] = {};
   {
     std::lock_guard<std::mutex> g(mu);
     if (di->device < 64 && !configured[di->device]) {
-      cudaError_t e = cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)di->max_smem_per_block_optin);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(layout_kernel)");
+      for (auto k : {layout_kernel<8>, layout_kernel<EP_MAX_TOPK>}) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)di->max_smem_per_block_optin);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(layout_kernel)");
+      }
       configured[di->device] = true;
     }
   }
@@ -270,7 +297,7 @@ ep_status_t launch_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
                   "ep_get_layout: %d tokens need %zu bytes of shared memory per block (max %zu)",
                   num_tokens, smem, di->max_smem_per_block_optin);
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layout_kernel, kLayoutThreads, smem);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kLayoutThreads, smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(layout)");
     const int cap = per_sm * di->num_sms;
     if (cap <= 0) return fail(EP_ERR_UNSUPPORTED, "ep_get_layout: layout kernel cannot be resident");
@@ -291,17 +318,7 @@ ep_status_t launch_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
   p.bar = static_cast<BarrierWords *>(workspace);
   p.partial = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(workspace) + kPartialOffset);
 
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kLayoutThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, layout_kernel, p);
+  cudaError_t e = launch_kernel(kernel, grid, kLayoutThreads, smem, stream, true, p);
   if (e != cudaSuccess) return cuda_fail(e, "launch layout_kernel");
   return EP_OK;
 }
