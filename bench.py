@@ -65,7 +65,15 @@ KERNEL_SOURCES = {
     "dispatch": ["ep_dispatch.cu", "ep_device.cuh"],
     "combine": ["ep_combine.cu", "ep_device.cuh"],
 }
-KERNEL_SYMBOL = {"layout": "layout_kernel", "dispatch": "dispatch_kernel", "combine": "combine_kernel"}
+def kernel_symbol(kernel: str, cfg: W.EPConfig) -> str:
+    """The library kernel that runs each call for this workload (the library
+    picks the warp-specialised fp8 dispatch, the ring kernel for bf16, and
+    the warp-specialised combine for up to 8 ranks)."""
+    if kernel == "layout":
+        return "layout_kernel"
+    if kernel == "dispatch":
+        return "dispatch_ws_kernel" if cfg.fp8 else "dispatch_ring_kernel"
+    return "combine_ws_kernel" if cfg.num_ranks <= 8 else "combine_kernel"
 
 
 def kernel_source_hash(kernel: str) -> str:
@@ -76,7 +84,7 @@ def kernel_source_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, workload: str):
+def ncu_traffic(kernel: str, cfg: W.EPConfig):
     """DRAM bytes per launch from the committed ncu summary, or None when
     there is none or the kernel's source changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "ncu_dram_traffic.txt")
@@ -84,7 +92,7 @@ def ncu_traffic(kernel: str, workload: str):
         return None
     for line in open(path):
         f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
-        if f.get("kernel") == KERNEL_SYMBOL[kernel] and f.get("workload") == workload:
+        if f.get("kernel") == kernel_symbol(kernel, cfg) and f.get("workload") == cfg.name:
             if f.get("source_sha256") != kernel_source_hash(kernel):
                 return None
             return int(f["dram_bytes_per_launch"])
@@ -370,9 +378,9 @@ def run_ours(args, rank, world, local):
                        "frac_of_" + peak_kind + "_peak": round(gbs / peak, 4)}
     dom = max(names, key=lambda nm: per_kernel_ms[nm])
     dom_gbs = abytes[dom] / (per_kernel_ms[dom] * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": KERNEL_SYMBOL[dom], "achieved": round(dom_gbs, 1),
+    roofline = {"bound": "hbm", "kernel": kernel_symbol(dom, cfg), "achieved": round(dom_gbs, 1),
                 "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                "frac": round(dom_gbs / peak, 4), "traffic": ncu_traffic(dom, cfg.name),
+                "frac": round(dom_gbs / peak, 4), "traffic": ncu_traffic(dom, cfg),
                 "algorithmic_bytes_per_launch": abytes[dom]}
     step_bytes = sum(abytes.values())
     step_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9

@@ -98,6 +98,14 @@ __device__ __forceinline__ void bulk_store(void *dst_gmem, const void *src_smem,
                : "memory");
 }
 
+// Same, with an L2 eviction-priority policy (from createpolicy).
+__device__ __forceinline__ void bulk_store_hint(void *dst_gmem, const void *src_smem, uint32_t bytes,
+                                                uint64_t policy) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst_gmem),
+               "r"(smem_addr(src_smem)), "r"(bytes), "l"(policy)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

@@ -25,7 +25,7 @@
 namespace ep {
 namespace {
 
-constexpr int kLayoutThreads = 128;  // one token per thread per chunk
+constexpr int kLayoutThreads = 256;  // one token per thread per chunk
 constexpr int kLayoutWarps = kLayoutThreads / kWarpSize;
 constexpr size_t kPartialOffset = 256;  // bytes: barrier words come first
 

@@ -151,7 +151,7 @@ ep_status_t ep_get_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
  *
  *   Limit: ep_layout_workspace_bytes(T, E, R) must not exceed
  *   EP_NOALLOC_SCRATCH_BYTES, else EP_ERR_UNSUPPORTED (for R = 8 that is
- *   T <= 1,047,552 tokens; for R = 64, T <= 130,944).
+ *   T <= 2,095,104 tokens; for R = 64, T <= 261,888).
  *   Set-up: the first call on a device looks up the device address of the
  *   scratch array once (with that device current); make that first call
  *   before any stream capture.

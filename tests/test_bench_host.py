@@ -31,15 +31,16 @@ def test_traffic_lookup_needs_matching_source(tmp_path, monkeypatch):
     prof.mkdir()
     h = bench.kernel_source_hash("combine")
     (prof / "ncu_dram_traffic.txt").write_text(
-        f"kernel=combine_kernel workload=w1 dram_bytes_per_launch=123 source_sha256={h}\n"
-        f"kernel=dispatch_kernel workload=w1 dram_bytes_per_launch=7 source_sha256=stale\n")
+        f"kernel=combine_ws_kernel workload=w1 dram_bytes_per_launch=123 source_sha256={h}\n"
+        f"kernel=dispatch_ws_kernel workload=w1 dram_bytes_per_launch=7 source_sha256=stale\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     # kernel_source_hash reads the sources under ROOT: point it back
     monkeypatch.setattr(bench, "kernel_source_hash",
                         lambda k, _h=bench.kernel_source_hash: {"combine": h}.get(k, "x"))
-    assert bench.ncu_traffic("combine", "w1") == 123
-    assert bench.ncu_traffic("dispatch", "w1") is None       # stale source
-    assert bench.ncu_traffic("combine", "other") is None
+    cfg = W.CONFIGS["fp8_8192x7168_top8_256e"].with_(name="w1")
+    assert bench.ncu_traffic("combine", cfg) == 123
+    assert bench.ncu_traffic("dispatch", cfg) is None        # stale source
+    assert bench.ncu_traffic("combine", cfg.with_(name="other")) is None
 
 
 def _free_port():
