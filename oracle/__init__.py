@@ -29,6 +29,7 @@ _LIB = os.path.join(_HERE, "libep_oracle.so")
 
 BAD_INDEX = 1
 CAPACITY = 2
+STALE = 8
 
 _lock = threading.Lock()
 _default = None

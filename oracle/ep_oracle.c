@@ -28,12 +28,19 @@
  *   [TS-STATS]  same page, commit message adding cumulative recv stats and
  *               combine bias: recv_topk_idx holds the local expert of every
  *               received (row, top-k slot).
+ *   [TS-CACHE]  same page, commit messages on the cached-layout dispatch
+ *               (handle=): a layout depends only on the routing; a stale one
+ *               misroutes silently, so it is guarded.
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *   - expert e lives on rank floor(e / (E/R)) (contiguous blocks).
  *   - slots inside a rank are claimed in ascending token order (stable).
  *   - received rows are rank-major: rank 0's block, then rank 1's, ...
  *   - an index outside [-1, E) is treated as -1 and flags EP_ORA_BAD_INDEX.
+ *   - stale layout: dispatch and weighted combine flag EP_ORA_STALE for a
+ *     token whose set of ranks under the routing they are given differs
+ *     from the ranks with a slot in the layout (the slots depend on nothing
+ *     else, so a routing with the same rank sets may reuse the layout).
  *   - fp8: amax = max |x| over the group, scale = amax / 448 (fp32 division,
  *     round to nearest even), q = e4m3(x / scale) rounded to nearest even
  *     with saturation at +-448; an all-zero group has scale 0 and keeps the
@@ -53,6 +60,7 @@
 
 #define EP_ORA_BAD_INDEX 1
 #define EP_ORA_CAPACITY 2
+#define EP_ORA_STALE 8      /* routing and layout disagree on a token's ranks */
 
 /* ------------------------------------------------------------------ */
 /* Number formats                                                      */
@@ -229,6 +237,24 @@ int ora_get_layout(const int64_t *topk_idx, int T, int K, int E, int R,
     return err;
 }
 
+/* 1 if token t's ranks under topk_idx are exactly its ranks with a slot. */
+static int ranks_agree(const int64_t *topk_idx, int t, int K, int E, int R,
+                       const int32_t *token_slot)
+{
+    int epr = E / R;
+    for (int r = 0; r < R; ++r) {
+        int routed = 0;
+        for (int k = 0; k < K; ++k) {
+            int64_t e = topk_idx[(size_t)t * K + k];
+            if (valid_expert(e, E) && (int)(e / epr) == r)
+                routed = 1;
+        }
+        if (routed != (token_slot[(size_t)t * R + r] >= 0))
+            return 0;
+    }
+    return 1;
+}
+
 /* ------------------------------------------------------------------ */
 /* Dispatch: scatter (bf16 or fp8) plus received metadata               */
 /* ------------------------------------------------------------------ */
@@ -257,6 +283,8 @@ int ora_dispatch(const uint16_t *x, int T, int H, const int64_t *topk_idx,
     for (int t = 0; t < T; ++t) {
         const uint16_t *row = x + (size_t)t * H;
         int quantised = 0;
+        if (!ranks_agree(topk_idx, t, K, E, R, token_slot))
+            err |= EP_ORA_STALE;
         for (int r = 0; r < R; ++r) {
             int32_t slot = token_slot[(size_t)t * R + r];
             if (slot < 0)
@@ -312,6 +340,8 @@ int ora_combine(const uint16_t *y, int cap, int H, const int32_t *token_slot,
     int epr = (R > 0) ? E / R : 0;
     float *acc = (float *)malloc(sizeof(float) * (size_t)(H > 0 ? H : 1));
     for (int t = 0; t < T; ++t) {
+        if (topk_weights && !ranks_agree(topk_idx, t, K, E, R, token_slot))
+            err |= EP_ORA_STALE;
         for (int h = 0; h < H; ++h)
             acc[h] = 0.0f;
         for (int r = 0; r < R; ++r) {

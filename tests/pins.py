@@ -481,4 +481,39 @@ def check_combine_rank_order(o):
     assert np.all(bits_to_f32(out) == 1.0)
 
 
+
+
+# ------------------------------------------------------------ stale layout
+
+def check_stale_layout_flag(o):
+    """A layout reused with another routing is flagged exactly when some
+    token's rank set changed; a routing with the same rank sets (experts
+    swapped within their ranks) reuses it and matches a fresh layout."""
+    g = _golden("layout_dispatch_combine_hand.json")
+    E, R = g["num_experts"], g["num_ranks"]
+    idx = np.array(g["topk_idx"], np.int64)
+    w = np.array(g["topk_weights"], np.float32)
+    _, bits = _hand_inputs()
+    lay = o.get_layout(idx, E, R)
+    d = o.dispatch(bits, idx, w, E, R, lay["token_slot"], False, 7)
+    assert d["error"] == 0
+    # same rank sets: expert 0 <-> 1 (rank 0), 6 <-> 7 (rank 3)
+    swap = {0: 1, 1: 0, 6: 7, 7: 6}
+    same = np.vectorize(lambda e: swap.get(int(e), int(e)))(idx).astype(np.int64)
+    d2 = o.dispatch(bits, same, w, E, R, lay["token_slot"], False, 7)
+    fresh = o.dispatch(bits, same, w, E, R, o.get_layout(same, E, R)["token_slot"], False, 7)
+    assert d2["error"] == 0
+    for k in ("recv_x", "recv_src_idx", "recv_topk_idx"):
+        assert np.array_equal(d2[k], fresh[k])
+    # token 2 (no selection) now picks expert 2 (rank 1): its rank set changed
+    moved = idx.copy()
+    moved[2, 0] = 2
+    d3 = o.dispatch(bits, moved, w, E, R, lay["token_slot"], False, 7)
+    assert d3["error"] & 8
+    _, err = o.combine(bits[np.array(g["expected"]["recv_src_idx"])], lay["token_slot"], moved, w, E)
+    assert err & 8
+    _, err = o.combine(bits[np.array(g["expected"]["recv_src_idx"])], lay["token_slot"], same, w, E)
+    assert err == 0
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

@@ -71,6 +71,8 @@ MUTANTS = [
      "acc[h] = acc[h] + p;", "acc[h] = acc[h] - p;"),
     ("combine_all_weights", "int ora_combine",
      "if (valid_expert(e, E) && (int)(e / epr) == r)", "if (valid_expert(e, E))"),
+    ("stale_check_inverted", "static int ranks_agree",
+     "if (routed != (token_slot[(size_t)t * R + r] >= 0))", "if (routed == (token_slot[(size_t)t * R + r] >= 0))"),
     ("combine_skips_rank0", "int ora_combine",
      "if (slot < 0)\n                continue;", "if (slot <= 0)\n                continue;"),
 ]
