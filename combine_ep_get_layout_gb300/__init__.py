@@ -22,7 +22,7 @@ import torch
 
 from . import _native as N
 from ._native import (EP_ERRBIT_BAD_INDEX, EP_ERRBIT_CAPACITY,  # noqa: F401
-                      EP_ERRBIT_TIMEOUT, EP_FP8_GROUP)
+                      EP_ERRBIT_STALE_LAYOUT, EP_ERRBIT_TIMEOUT, EP_FP8_GROUP)
 
 __all__ = ["EPError", "Layout", "Dispatched", "ep_layout_workspace_bytes",
            "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch", "ep_combine",

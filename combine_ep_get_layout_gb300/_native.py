@@ -23,6 +23,7 @@ EP_DTYPE_FP8_E4M3 = 1
 EP_ERRBIT_BAD_INDEX = 0x1
 EP_ERRBIT_CAPACITY = 0x2
 EP_ERRBIT_TIMEOUT = 0x4
+EP_ERRBIT_STALE_LAYOUT = 0x8
 
 EP_MAX_RANKS = 64
 EP_MAX_TOPK = 32

@@ -71,6 +71,13 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
   for (int t = blockIdx.x; t < p.T; t += gridDim.x, ++i) {
     const int b = i & 1;
     if (warp == 0) {
+      if (WEIGHTED) {
+        const int64_t e = lane < p.K ? __ldg(p.topk_idx + (size_t)t * p.K + lane) : -1;
+        const int lo = lane < p.R ? __ldg(p.token_slot + (size_t)t * p.R + lane) : -1;
+        const int hi = lane + kWarpSize < p.R ? __ldg(p.token_slot + (size_t)t * p.R + lane + kWarpSize) : -1;
+        if (!ranks_agree(e, p.E, p.epr, p.R, lo, hi, lane) && lane == 0)
+          set_error(p.error_word, EP_ERRBIT_STALE_LAYOUT);
+      }
       int count = 0;
       for (int r0 = 0; r0 < p.R; r0 += kWarpSize) {
         const int r = r0 + lane;
@@ -221,6 +228,8 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
       TokenMeta nxt = cur;
       if (j + 1 < ntok) nxt = fetch_meta(p, t + gridDim.x, lane, WEIGHTED);  // in flight meanwhile
       int slot = cur.slot;
+      if (WEIGHTED && !ranks_agree(cur.e, p.E, p.epr, p.R, slot, -1, lane) && lane == 0)
+        set_error(p.error_word, EP_ERRBIT_STALE_LAYOUT);
       if (slot >= p.cap) {
         set_error(p.error_word, EP_ERRBIT_CAPACITY);
         slot = -1;

@@ -188,6 +188,22 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Warp-collective: whether a token's set of ranks under its routing (expert
+// id `e` in lanes k < K, -1 in the other lanes) is exactly its set of ranks
+// with a slot (`slot_lo` = slot of rank `lane`, `slot_hi` = of rank
+// lane + 32, -1 where absent).  A layout depends on nothing else, so this
+// detects a layout computed for another routing.
+__device__ __forceinline__ bool ranks_agree(int64_t e, int E, int epr, int R, int slot_lo, int slot_hi,
+                                            int lane) {
+  const uint64_t bit = (e >= 0 && e < E) ? (1ull << (static_cast<int>(e) / epr)) : 0ull;
+  const uint64_t mask = (uint64_t)__reduce_or_sync(0xffffffffu, (uint32_t)bit) |
+                        ((uint64_t)__reduce_or_sync(0xffffffffu, (uint32_t)(bit >> 32)) << 32);
+  bool ok = true;
+  if (lane < R) ok = (((mask >> lane) & 1ull) != 0) == (slot_lo >= 0);
+  if (lane + 32 < R) ok = ok && ((((mask >> (lane + 32)) & 1ull) != 0) == (slot_hi >= 0));
+  return __all_sync(0xffffffffu, ok);
+}
+
 __device__ __forceinline__ void set_error(uint32_t *word, uint32_t bits) {
   if (word != nullptr) atomicOr(word, bits);
 }

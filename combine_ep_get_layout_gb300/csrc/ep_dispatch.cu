@@ -72,6 +72,14 @@ __device__ __forceinline__ void write_metadata(const DispatchParams &p, int t,
                                                const int32_t *slots, const float *scales) {
   const int mt = threadIdx.x - kWarpSize;
   const int nt = kDispatchThreads - kWarpSize;
+  if (threadIdx.x / kWarpSize == 1) {  // warp 1 checks the layout against the routing
+    const int lane = threadIdx.x & (kWarpSize - 1);
+    const int64_t e = lane < p.K ? __ldg(p.topk_idx + (size_t)t * p.K + lane) : -1;
+    const int lo = lane < p.R ? slots[lane] : -1;
+    const int hi = lane + kWarpSize < p.R ? slots[lane + kWarpSize] : -1;
+    if (!ranks_agree(e, p.E, p.epr, p.R, lo, hi, lane) && lane == 0)
+      set_error(p.error_word, EP_ERRBIT_STALE_LAYOUT);
+  }
   if (p.recv_src_idx != nullptr) {
     for (int j = mt; j < p.R; j += nt) {
       const int slot = slots[j];
@@ -324,6 +332,9 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
       const int32_t *srow = p.token_slot + (size_t)t * p.R;
       int slot_lo = lane < p.R ? __ldg(srow + lane) : -1;
       int slot_hi = lane + kWarpSize < p.R ? __ldg(srow + lane + kWarpSize) : -1;
+      const int64_t e = lane < p.K ? __ldg(p.topk_idx + (size_t)t * p.K + lane) : -1;
+      if (!ranks_agree(e, p.E, p.epr, p.R, slot_lo, slot_hi, lane) && lane == 0)
+        set_error(p.error_word, EP_ERRBIT_STALE_LAYOUT);
       if (slot_lo >= p.cap) {
         set_error(p.error_word, EP_ERRBIT_CAPACITY);
         slot_lo = -1;
@@ -332,7 +343,6 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
         set_error(p.error_word, EP_ERRBIT_CAPACITY);
         slot_hi = -1;
       }
-      const int64_t e = lane < p.K ? __ldg(p.topk_idx + (size_t)t * p.K + lane) : -1;
       const float w = (lane < p.K && p.recv_topk_weights != nullptr)
                           ? __ldg(p.topk_weights + (size_t)t * p.K + lane) : 0.0f;
       // received metadata: needs no shared memory, runs ahead of the cast

@@ -63,6 +63,8 @@ typedef enum {
 #define EP_ERRBIT_BAD_INDEX 0x1u  /* a topk_idx entry outside [-1, E)        */
 #define EP_ERRBIT_CAPACITY 0x2u   /* a row's slot >= recv_capacity: skipped  */
 #define EP_ERRBIT_TIMEOUT 0x4u    /* a bounded device wait gave up           */
+#define EP_ERRBIT_STALE_LAYOUT 0x8u /* routing and layout disagree on a token's
+                                       set of ranks (a layout of another routing) */
 
 /* Limits of this implementation (EP_ERR_UNSUPPORTED beyond them). */
 #define EP_MAX_RANKS 64
@@ -199,6 +201,14 @@ ep_status_t ep_get_layout_noalloc(const int64_t *topk_idx, int num_tokens, int n
  *                EP_ERRBIT_CAPACITY; T*min(K,R) always suffices.
  *   Rows [N, recv_capacity) are not written.
  *   1 <= H <= EP_MAX_HIDDEN.
+ *
+ * Cached layouts: a layout depends only on each token's set of ranks, so it
+ * may be reused for any routing with the same rank sets (TileScale PR #68,
+ * commit messages on the cached-layout dispatch: the notify phase is skipped
+ * when the routing is unchanged).  A stale layout would misroute silently;
+ * here every call compares each token's rank set under `topk_idx` with the
+ * ranks that have a slot and sets EP_ERRBIT_STALE_LAYOUT on a mismatch (the
+ * rows are still written where the layout says).
  */
 ep_status_t ep_dispatch(const void *x, int num_tokens, int hidden,
                         const int64_t *topk_idx, const float *topk_weights,
@@ -231,6 +241,8 @@ ep_status_t ep_dispatch(const void *x, int num_tokens, int hidden,
  *   layout   the layout the rows were dispatched with.
  *   topk_idx, topk_weights: [T*K] device, or both NULL for the plain sum.
  *   out      [T*H] bf16, device, 16-byte aligned.  H % 8 == 0.
+ *   With weights, a token whose rank set under topk_idx differs from the
+ *   layout's sets EP_ERRBIT_STALE_LAYOUT (see ep_dispatch).
  */
 ep_status_t ep_combine(const void *y, int recv_capacity, int hidden,
                        const ep_layout_t *layout, int num_tokens, int num_ranks,

@@ -236,3 +236,62 @@ def test_workspace_reuse_across_sizes_and_streams():
         main.wait_stream(s)
         torch.cuda.synchronize()
         U.assert_layout_equal(U.layout_np(lay), oracle.get_layout(idx, E, R))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_cached_layout_and_stale_guard(dtype):
+    """Fresh, cached and cached-twice dispatches agree; a routing with the
+    same rank sets reuses the layout cleanly (and matches a fresh layout);
+    a routing whose rank sets changed is flagged by dispatch and by the
+    weighted combine (TileScale PR #68: a stale handle must not misroute
+    silently)."""
+    cfg = W.CONFIGS["bf16_4096x4096_top6_64e"]
+    inp = W.make(cfg)
+    E, R = cfg.num_experts, cfg.num_ranks
+    epr = E // R
+    x = U.to_dev_bf16(inp["x"])
+    w = torch.from_numpy(inp["topk_weights"]).to(U.dev())
+    idx_np = inp["topk_idx"]
+    idx = torch.from_numpy(idx_np).to(U.dev())
+    lay = ep.ep_get_layout(idx, E, R)
+    runs = [ep.ep_dispatch(x, idx, w, lay, dtype=dtype) for _ in range(3)]  # fresh, cached, cached twice
+    torch.cuda.synchronize()
+    assert lay.errors() == 0
+    N = lay.num_recv()
+    for d in runs[1:]:
+        assert torch.equal(d.recv_x.view(torch.uint8)[:N], runs[0].recv_x.view(torch.uint8)[:N])
+        assert torch.equal(d.recv_topk_idx[:N], runs[0].recv_topk_idx[:N])
+
+    # experts permuted inside their ranks: same rank sets, same slots
+    same_np = ((idx_np // epr) * epr + (idx_np % epr + 3) % epr).astype(np.int64)
+    same = torch.from_numpy(same_np).to(U.dev())
+    d_cached = ep.ep_dispatch(x, same, w, lay, dtype=dtype)
+    out_cached = ep.ep_combine(U.to_dev_bf16(U.bits(d_cached.recv_x)) if dtype == "bf16" else
+                               U.to_dev_bf16(W.expert_output(d_cached.recv_x.shape[0], cfg.hidden)),
+                               lay, same, w)
+    torch.cuda.synchronize()
+    assert lay.errors() == 0
+    lay2 = ep.ep_get_layout(same, E, R)
+    d_fresh = ep.ep_dispatch(x, same, w, lay2, dtype=dtype)
+    torch.cuda.synchronize()
+    assert torch.equal(lay2.token_slot, lay.token_slot)
+    assert torch.equal(d_fresh.recv_x.view(torch.uint8)[:N], d_cached.recv_x.view(torch.uint8)[:N])
+    assert torch.equal(d_fresh.recv_topk_idx[:N], d_cached.recv_topk_idx[:N])
+
+    # some tokens now reach another rank: flagged by dispatch and combine
+    moved_np = idx_np.copy()
+    moved_np[:16, 0] = (moved_np[:16, 0] + epr) % E
+    changed = [set((moved_np[t] // epr).tolist()) != set((idx_np[t] // epr).tolist()) for t in range(16)]
+    assert any(changed)
+    moved = torch.from_numpy(moved_np).to(U.dev())
+    ep.ep_dispatch(x, moved, w, lay, dtype=dtype)
+    torch.cuda.synchronize()
+    assert lay.errors() & ep.EP_ERRBIT_STALE_LAYOUT
+    lay.error_word.zero_()
+    ep.ep_combine(U.to_dev_bf16(W.expert_output(lay.num_recv(), cfg.hidden)), lay, moved, w)
+    torch.cuda.synchronize()
+    assert lay.errors() & ep.EP_ERRBIT_STALE_LAYOUT
+    # the oracle agrees on which case is stale
+    o = oracle.dispatch(inp["x"], moved_np, inp["topk_weights"], E, R, U.bits(lay.token_slot),
+                        False, N)
+    assert o["error"] & oracle.STALE
