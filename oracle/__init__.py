@@ -72,6 +72,12 @@ def _bind(path: str):
     L.ora_dispatch.restype = i
     L.ora_combine.argtypes = [p, i, i, p, i, i, p, p, i, i, p]
     L.ora_combine.restype = i
+    L.ora_dispatch_ex.argtypes = [p, i, i, p, p, i, i, i, p, i, p, p, p, p, p, i, p]
+    L.ora_dispatch_ex.restype = i
+    L.ora_combine_ex.argtypes = [p, i, i, p, i, i, p, p, i, i, p, p, p]
+    L.ora_combine_ex.restype = i
+    L.ora_fp8_packed_row_bytes.argtypes = [i]
+    L.ora_fp8_packed_row_bytes.restype = i
     return L
 
 
@@ -158,9 +164,16 @@ class Oracle:
         out["error"] = int(err)
         return out
 
+    def fp8_packed_row_bytes(self, hidden: int) -> int:
+        return int(self._L.ora_fp8_packed_row_bytes(int(hidden)))
+
     def dispatch(self, x_bits, topk_idx, topk_weights, num_experts: int,
-                 num_ranks: int, token_slot, fp8: bool,
-                 recv_capacity: int) -> dict:
+                 num_ranks: int, token_slot, fp8, recv_capacity: int,
+                 stats=None) -> dict:
+        """fp8: False (bf16 rows), True (e4m3 rows + separate scales) or
+        "packed" (e4m3 codes, scales and zero padding in one row).
+        ``stats`` (uint32 [E]) is accumulated in place when given."""
+        mode = 2 if fp8 == "packed" else (1 if fp8 else 0)
         x = _c(x_bits, np.uint16)
         idx = _c(topk_idx, np.int64)
         w = _c(topk_weights, np.float32)
@@ -169,18 +182,21 @@ class Oracle:
         K = idx.shape[1]
         cap = int(recv_capacity)
         G = H // 128
+        width = H if mode < 2 else self.fp8_packed_row_bytes(H)
         # one guard row past the capacity: it must come back untouched
-        recv_x = np.zeros((cap + 1, H), np.uint8 if fp8 else np.uint16)
-        scales = np.zeros((cap + 1, G), np.float32) if fp8 else None
+        recv_x = np.zeros((cap + 1, width), np.uint8 if mode else np.uint16)
+        scales = np.zeros((cap + 1, G), np.float32) if mode == 1 else None
         src = np.full(cap + 1, -7, np.int32)
         ridx = np.full((cap + 1, K), -7, np.int32)
         rw = np.full((cap + 1, K), np.nan, np.float32)
-        err = self._L.ora_dispatch(
+        if stats is not None:
+            assert stats.dtype == np.uint32 and stats.flags.c_contiguous
+        err = self._L.ora_dispatch_ex(
             _ptr(x), T, H, _ptr(idx), _ptr(w), K, num_experts, num_ranks,
-            _ptr(slot), 1 if fp8 else 0, _ptr(recv_x), _ptr(scales), _ptr(src),
-            _ptr(ridx), _ptr(rw), cap)
+            _ptr(slot), mode, _ptr(recv_x), _ptr(scales), _ptr(src),
+            _ptr(ridx), _ptr(rw), cap, _ptr(stats))
         if (src[cap] != -7 or np.any(ridx[cap] != -7) or np.any(recv_x[cap])
-                or (fp8 and np.any(scales[cap]))):
+                or (mode == 1 and np.any(scales[cap]))):
             raise AssertionError("dispatch wrote past its capacity")
         return {"recv_x": recv_x[:cap],
                 "recv_x_scales": None if scales is None else scales[:cap],
@@ -188,7 +204,7 @@ class Oracle:
                 "recv_topk_weights": rw[:cap], "error": int(err)}
 
     def combine(self, y_bits, token_slot, topk_idx=None, topk_weights=None,
-                num_experts: int = 0) -> tuple[np.ndarray, int]:
+                num_experts: int = 0, bias0=None, bias1=None) -> tuple[np.ndarray, int]:
         """out bf16 bits [T, H] and error bits."""
         y = _c(y_bits, np.uint16)
         slot = _c(token_slot, np.int32)
@@ -198,9 +214,12 @@ class Oracle:
         idx = _c(topk_idx, np.int64) if weighted else None
         w = _c(topk_weights, np.float32) if weighted else None
         K = idx.shape[1] if weighted else 0
+        b0 = None if bias0 is None else _c(bias0, np.uint16)
+        b1 = None if bias1 is None else _c(bias1, np.uint16)
         out = np.empty((T, H), np.uint16)
-        err = self._L.ora_combine(_ptr(y), cap, H, _ptr(slot), T, R,
-                                  _ptr(idx), _ptr(w), K, num_experts, _ptr(out))
+        err = self._L.ora_combine_ex(_ptr(y), cap, H, _ptr(slot), T, R,
+                                     _ptr(idx), _ptr(w), K, num_experts,
+                                     _ptr(b0), _ptr(b1), _ptr(out))
         return out, int(err)
 
     def run_path(self, inputs: dict, num_experts: int, num_ranks: int,
@@ -239,5 +258,6 @@ def _forward(name):
 
 
 for _n in ("bf16_to_f32", "f32_to_bf16", "e4m3_to_f64", "f32_to_e4m3",
-           "quantize_row", "get_layout", "dispatch", "combine", "run_path"):
+           "quantize_row", "fp8_packed_row_bytes", "get_layout", "dispatch",
+           "combine", "run_path"):
     globals()[_n] = _forward(_n)

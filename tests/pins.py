@@ -516,4 +516,103 @@ def check_stale_layout_flag(o):
     assert err == 0
 
 
+# ------------------------------------------- packed rows, stats, combine bias
+
+def check_packed_row_sizes_golden(o):
+    g = _golden("fp8_packed_row_sizes.json")
+    for c in g["cases"]:
+        H = c["hidden"]
+        raw = H + 4 * (H // 128)
+        if c["raw_bytes"] is not None:
+            assert raw == c["raw_bytes"]
+        rb = o.fp8_packed_row_bytes(H)
+        pad512 = -(-raw // 512) * 512
+        if c["pct_512_padding"] is not None:
+            printed = str(c["pct_512_padding"])   # compared at the precision the page prints
+            digits = len(printed.split(".")[1]) if "." in printed else 0
+            assert round(100 * (pad512 - raw) / raw, digits) == c["pct_512_padding"]
+        assert (rb == pad512) == c["uses_512"]
+        assert rb % 16 == 0 and rb >= raw and (c["uses_512"] or rb - raw < 16)
+        if "row_bytes" in c:
+            assert rb == c["row_bytes"]
+
+
+def check_packed_rows(o):
+    rng = np.random.default_rng(51)
+    for T, H, K, E, R in [(200, 7168, 8, 256, 8), (150, 128, 3, 12, 3), (90, 640, 4, 16, 4)]:
+        idx = _random_idx(rng, T, K, E, p_mask=0.1)
+        w = rng.random((T, K)).astype(np.float32)
+        x = bf16_bits(rng.standard_normal((T, H)).astype(np.float32)).reshape(T, H)
+        lay = o.get_layout(idx, E, R)
+        N = int(lay["rank_prefix"][R])
+        sep = o.dispatch(x, idx, w, E, R, lay["token_slot"], True, N)
+        pk = o.dispatch(x, idx, w, E, R, lay["token_slot"], "packed", N)
+        rb = o.fp8_packed_row_bytes(H)
+        assert pk["recv_x"].shape == (N, rb) and pk["recv_x_scales"] is None
+        assert np.array_equal(pk["recv_x"][:, :H], sep["recv_x"])
+        assert np.array_equal(pk["recv_x"][:, H:H + 4 * (H // 128)].view(np.float32), sep["recv_x_scales"])
+        assert not pk["recv_x"][:, H + 4 * (H // 128):].any()
+        for k in ("recv_src_idx", "recv_topk_idx"):
+            assert np.array_equal(pk[k], sep[k])
+
+
+def check_recv_stats(o):
+    """Three accumulating dispatches with a quarter of the selections masked:
+    the stats are three times the per-expert counts of valid selections."""
+    rng = np.random.default_rng(52)
+    T, H, K, E, R = 300, 64, 6, 32, 4
+    stats = np.full(E, 5, np.uint32)
+    idx = _random_idx(rng, T, K, E, p_mask=0.25)
+    w = rng.random((T, K)).astype(np.float32)
+    x = bf16_bits(rng.standard_normal((T, H)).astype(np.float32)).reshape(T, H)
+    lay = o.get_layout(idx, E, R)
+    N = int(lay["rank_prefix"][R])
+    for _ in range(3):
+        o.dispatch(x, idx, w, E, R, lay["token_slot"], False, N, stats=stats)
+    counts = np.bincount(idx[idx >= 0], minlength=E)
+    assert np.array_equal(stats, 5 + 3 * counts)
+
+
+def check_combine_bias(o):
+    rng = np.random.default_rng(53)
+    T, H, K, E, R = 120, 64, 4, 16, 4
+    idx = _random_idx(rng, T, K, E, p_mask=0.3)
+    idx[:5] = -1                                        # fully masked tokens
+    w = rng.random((T, K)).astype(np.float32)
+    lay = o.get_layout(idx, E, R)
+    N = int(lay["rank_prefix"][R])
+    y = bf16_bits(rng.standard_normal((N, H)).astype(np.float32)).reshape(N, H)
+    b0 = bf16_bits(rng.standard_normal((T, H)).astype(np.float32)).reshape(T, H)
+    b1 = bf16_bits(rng.standard_normal((T, H)).astype(np.float32)).reshape(T, H)
+    b0[0, :4] = 0x8000                                  # -0 survives a seed
+    # one bias: a fully masked token comes back as its bias, bit for bit
+    out, _ = o.combine(y, lay["token_slot"], idx, w, E, bias0=b0)
+    assert np.array_equal(out[:5], b0[:5])
+    # two biases: bf16(b0 + b1) there (fp32 sum, rounded by torch)
+    out2, _ = o.combine(y, lay["token_slot"], idx, w, E, bias0=b0, bias1=b1)
+    s01 = bits_to_f32(b0[:5]).reshape(5, H) + bits_to_f32(b1[:5]).reshape(5, H)
+    ref = torch.from_numpy(s01.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(out2[:5], ref)
+    # elsewhere: the biased sum, within rounding of the exact fp64 value
+    plain, _ = o.combine(y, lay["token_slot"], idx, w, E)
+    yf = bits_to_f32(y).reshape(N, H).astype(np.float64)
+    epr = E // R
+    for t in range(5, T):
+        exact = bits_to_f32(b0[t]).astype(np.float64) + bits_to_f32(b1[t]).astype(np.float64)
+        absum = np.abs(exact).copy()
+        for r in range(R):
+            s_ = lay["token_slot"][t, r]
+            if s_ < 0:
+                continue
+            c = sum(float(w[t, k]) for k in range(K) if idx[t, k] >= 0 and idx[t, k] // epr == r)
+            exact += c * yf[s_]
+            absum += abs(c) * np.abs(yf[s_])
+        got = bits_to_f32(out2[t]).astype(np.float64)
+        assert np.all(np.abs(got - exact) <= 2.0 ** -8 * np.abs(exact) + 2.0 ** -18 * absum)
+    # no bias is the plain combine
+    out0, _ = o.combine(y, lay["token_slot"], idx, w, E, bias0=None, bias1=None)
+    assert np.array_equal(out0, plain)
+
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

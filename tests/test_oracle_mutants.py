@@ -73,6 +73,16 @@ MUTANTS = [
      "if (valid_expert(e, E) && (int)(e / epr) == r)", "if (valid_expert(e, E))"),
     ("stale_check_inverted", "static int ranks_agree",
      "if (routed != (token_slot[(size_t)t * R + r] >= 0))", "if (routed == (token_slot[(size_t)t * R + r] >= 0))"),
+    ("packed_threshold_10pct", "int ora_fp8_packed_row_bytes",
+     "(pad512 - raw) * 20 < raw", "(pad512 - raw) * 10 < raw"),
+    ("packed_scales_before_payload", "int ora_dispatch_ex",
+     "memcpy(dst + H, sc, sizeof(float) * (size_t)G);", "memcpy(dst, sc, sizeof(float) * (size_t)G);"),
+    ("stats_every_slot", "int ora_dispatch_ex",
+     "if (stats && here)", "if (stats)"),
+    ("bias1_ignored", "int ora_combine_ex",
+     "acc[h] = acc[h] + ora_bf16_to_f32(bias1[(size_t)t * H + h]);", "acc[h] = acc[h];"),
+    ("bias_added_after", "int ora_combine_ex",
+     "acc[h] = bias0 ? ora_bf16_to_f32(bias0[(size_t)t * H + h]) : 0.0f;", "acc[h] = 0.0f;"),
     ("combine_skips_rank0", "int ora_combine",
      "if (slot < 0)\n                continue;", "if (slot <= 0)\n                continue;"),
 ]
