@@ -25,8 +25,8 @@ from ._native import (EP_ERRBIT_BAD_INDEX, EP_ERRBIT_CAPACITY,  # noqa: F401
                       EP_ERRBIT_STALE_LAYOUT, EP_ERRBIT_TIMEOUT, EP_FP8_GROUP)
 
 __all__ = ["EPError", "Layout", "Dispatched", "ep_layout_workspace_bytes",
-           "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch", "ep_combine",
-           "library_path"]
+           "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch", "ep_dispatch_ex",
+           "ep_combine", "ep_combine_ex", "ep_fp8_packed_row_bytes", "library_path"]
 
 
 class EPError(RuntimeError):
@@ -68,6 +68,11 @@ def _want(t: torch.Tensor, name: str, dtype, device=None):
         raise ValueError(f"{name} is on {t.device}, expected {device}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def ep_fp8_packed_row_bytes(hidden: int) -> int:
+    """Bytes of one packed fp8 row (codes, scales, zero padding)."""
+    return int(N.load().ep_fp8_packed_row_bytes(hidden))
 
 
 def ep_layout_workspace_bytes(num_tokens: int, num_experts: int, num_ranks: int) -> int:
@@ -160,14 +165,24 @@ class Dispatched:
     recv_topk_weights: Optional[torch.Tensor]  # fp32 [cap, K]
 
 
+_DTYPES = {"bf16": N.EP_DTYPE_BF16, "fp8": N.EP_DTYPE_FP8_E4M3,
+           "fp8_packed": N.EP_DTYPE_FP8_E4M3_PACKED}
+
+
 def ep_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: Optional[torch.Tensor],
                 layout: Layout, dtype: str = "bf16", recv_capacity: Optional[int] = None,
                 out: Optional[Dispatched] = None, metadata: bool = True,
+                cumulative_recv_stats: Optional[torch.Tensor] = None,
                 stream=None) -> Dispatched:
     """Scatter rows of ``x`` (bf16 [T, H]) to their received slots.
 
-    ``dtype`` is "bf16" or "fp8".  Without ``recv_capacity`` the buffers are
-    sized T * min(K, R), which needs no read-back of the layout.
+    ``dtype`` is "bf16", "fp8" (e4m3 rows + a separate scale array) or
+    "fp8_packed" (codes, scales and padding in one uint8 row of
+    ``ep_fp8_packed_row_bytes(H)`` bytes).  Without ``recv_capacity`` the
+    buffers are sized T * min(K, R), which needs no read-back of the layout.
+    ``cumulative_recv_stats`` (uint32 [E]) is accumulated in place.  The
+    plain C entry point ep_dispatch serves the options it has; the others go
+    through ep_dispatch_ex.
     """
     _want(x, "x", torch.bfloat16)
     dev = x.device
@@ -175,38 +190,71 @@ def ep_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: Optional[
     T, H = x.shape
     K = topk_idx.shape[1]
     E, R = layout.num_experts, layout.num_ranks
-    fp8 = {"bf16": False, "fp8": True}[dtype]
+    code = _DTYPES[dtype]
+    fp8 = code != N.EP_DTYPE_BF16
+    packed = code == N.EP_DTYPE_FP8_E4M3_PACKED
     if recv_capacity is None:
         recv_capacity = out.recv_x.shape[0] if out is not None else T * min(K, R)
     if out is None:
+        if packed:
+            rx = torch.empty((recv_capacity, ep_fp8_packed_row_bytes(H)), dtype=torch.uint8, device=dev)
+        else:
+            rx = torch.empty((recv_capacity, H), dtype=torch.float8_e4m3fn if fp8 else torch.bfloat16,
+                             device=dev)
         out = Dispatched(
-            torch.empty((recv_capacity, H), dtype=torch.float8_e4m3fn if fp8 else torch.bfloat16, device=dev),
-            torch.empty((recv_capacity, H // EP_FP8_GROUP), dtype=torch.float32, device=dev) if fp8 else None,
+            rx,
+            torch.empty((recv_capacity, H // EP_FP8_GROUP), dtype=torch.float32, device=dev)
+            if fp8 and not packed else None,
             torch.empty(recv_capacity, dtype=torch.int32, device=dev) if metadata else None,
             torch.empty((recv_capacity, K), dtype=torch.int32, device=dev) if metadata else None,
             torch.empty((recv_capacity, K), dtype=torch.float32, device=dev)
             if metadata and topk_weights is not None else None)
     if topk_weights is not None:
         _want(topk_weights, "topk_weights", torch.float32, dev)
-    _want(out.recv_x, "recv_x", torch.float8_e4m3fn if fp8 else torch.bfloat16, dev)
+    _want(out.recv_x, "recv_x",
+          torch.uint8 if packed else torch.float8_e4m3fn if fp8 else torch.bfloat16, dev)
     if out.recv_x.shape[0] < recv_capacity:
         raise ValueError("recv_x has fewer rows than recv_capacity")
+    if cumulative_recv_stats is not None:
+        if cumulative_recv_stats.dtype not in (torch.int32, torch.uint32) or \
+                cumulative_recv_stats.numel() != E or not cumulative_recv_stats.is_cuda:
+            raise ValueError("cumulative_recv_stats must be a 32-bit CUDA tensor of num_experts entries")
     st = layout.c_struct()
-    _check(N.load().ep_dispatch(
-        _ptr(x), T, H, _ptr(topk_idx), _ptr(topk_weights), K, E, R, C.byref(st),
-        N.EP_DTYPE_FP8_E4M3 if fp8 else N.EP_DTYPE_BF16, _ptr(out.recv_x),
-        _ptr(out.recv_x_scales), _ptr(out.recv_src_idx), _ptr(out.recv_topk_idx),
-        _ptr(out.recv_topk_weights), recv_capacity, _stream(stream, dev)), "ep_dispatch")
+    lib = N.load()
+    if packed or cumulative_recv_stats is not None:
+        args = N.ep_dispatch_args_t(
+            x.data_ptr(), T, H, topk_idx.data_ptr(),
+            None if topk_weights is None else topk_weights.data_ptr(), K, E, R,
+            C.pointer(st), code, out.recv_x.data_ptr(),
+            None if out.recv_x_scales is None else out.recv_x_scales.data_ptr(),
+            None if out.recv_src_idx is None else out.recv_src_idx.data_ptr(),
+            None if out.recv_topk_idx is None else out.recv_topk_idx.data_ptr(),
+            None if out.recv_topk_weights is None else out.recv_topk_weights.data_ptr(),
+            recv_capacity,
+            None if cumulative_recv_stats is None else cumulative_recv_stats.data_ptr())
+        _check(lib.ep_dispatch_ex(C.byref(args), _stream(stream, dev)), "ep_dispatch_ex")
+    else:
+        _check(lib.ep_dispatch(
+            _ptr(x), T, H, _ptr(topk_idx), _ptr(topk_weights), K, E, R, C.byref(st), code,
+            _ptr(out.recv_x), _ptr(out.recv_x_scales), _ptr(out.recv_src_idx),
+            _ptr(out.recv_topk_idx), _ptr(out.recv_topk_weights), recv_capacity,
+            _stream(stream, dev)), "ep_dispatch")
     return out
+
+
+ep_dispatch_ex = ep_dispatch
 
 
 def ep_combine(y: torch.Tensor, layout: Layout, topk_idx: Optional[torch.Tensor] = None,
                topk_weights: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+               bias0: Optional[torch.Tensor] = None, bias1: Optional[torch.Tensor] = None,
                stream=None) -> torch.Tensor:
-    """out[t] = bf16(sum over ranks r ascending of c[t,r] * y[token_slot[t,r]]).
+    """out[t] = bf16(bias0 + bias1 + sum over ranks r ascending of
+    c[t,r] * y[token_slot[t,r]]), accumulated in fp32 in that order.
 
     Without weights c = 1; with ``topk_idx``/``topk_weights`` c[t,r] is the
-    sum of t's gate weights on rank r.
+    sum of t's gate weights on rank r.  The biases (bf16 [T, H]) are
+    optional and go through ep_combine_ex.
     """
     _want(y, "y", torch.bfloat16)
     dev = y.device
@@ -219,11 +267,29 @@ def ep_combine(y: torch.Tensor, layout: Layout, topk_idx: Optional[torch.Tensor]
         _want(topk_idx, "topk_idx", torch.int64, dev)
         _want(topk_weights, "topk_weights", torch.float32, dev)
         K = topk_idx.shape[1]
+    for name, b in (("bias0", bias0), ("bias1", bias1)):
+        if b is not None:
+            _want(b, name, torch.bfloat16, dev)
+            if tuple(b.shape) != (T, H):
+                raise ValueError(f"{name} must be [num_tokens, hidden]")
     if out is None:
         out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     _want(out, "out", torch.bfloat16, dev)
     st = layout.c_struct()
-    _check(N.load().ep_combine(
-        _ptr(y), cap, H, C.byref(st), T, R, _ptr(topk_idx), _ptr(topk_weights), K,
-        layout.num_experts, _ptr(out), _stream(stream, dev)), "ep_combine")
+    lib = N.load()
+    if bias0 is not None or bias1 is not None:
+        args = N.ep_combine_args_t(
+            y.data_ptr(), cap, H, C.pointer(st), T, R,
+            None if topk_idx is None else topk_idx.data_ptr(),
+            None if topk_weights is None else topk_weights.data_ptr(), K, layout.num_experts,
+            None if bias0 is None else bias0.data_ptr(),
+            None if bias1 is None else bias1.data_ptr(), out.data_ptr())
+        _check(lib.ep_combine_ex(C.byref(args), _stream(stream, dev)), "ep_combine_ex")
+    else:
+        _check(lib.ep_combine(
+            _ptr(y), cap, H, C.byref(st), T, R, _ptr(topk_idx), _ptr(topk_weights), K,
+            layout.num_experts, _ptr(out), _stream(stream, dev)), "ep_combine")
     return out
+
+
+ep_combine_ex = ep_combine

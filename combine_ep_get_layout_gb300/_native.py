@@ -19,6 +19,7 @@ EP_ERR_CUDA = 3
 
 EP_DTYPE_BF16 = 0
 EP_DTYPE_FP8_E4M3 = 1
+EP_DTYPE_FP8_E4M3_PACKED = 2
 
 EP_ERRBIT_BAD_INDEX = 0x1
 EP_ERRBIT_CAPACITY = 0x2
@@ -44,6 +45,28 @@ class ep_layout_t(C.Structure):
     ]
 
 
+class ep_dispatch_args_t(C.Structure):
+    _fields_ = [
+        ("x", C.c_void_p), ("num_tokens", C.c_int), ("hidden", C.c_int),
+        ("topk_idx", C.c_void_p), ("topk_weights", C.c_void_p), ("num_topk", C.c_int),
+        ("num_experts", C.c_int), ("num_ranks", C.c_int),
+        ("layout", C.POINTER(ep_layout_t)), ("dtype", C.c_int),
+        ("recv_x", C.c_void_p), ("recv_x_scales", C.c_void_p), ("recv_src_idx", C.c_void_p),
+        ("recv_topk_idx", C.c_void_p), ("recv_topk_weights", C.c_void_p),
+        ("recv_capacity", C.c_int), ("cumulative_recv_stats", C.c_void_p),
+    ]
+
+
+class ep_combine_args_t(C.Structure):
+    _fields_ = [
+        ("y", C.c_void_p), ("recv_capacity", C.c_int), ("hidden", C.c_int),
+        ("layout", C.POINTER(ep_layout_t)), ("num_tokens", C.c_int), ("num_ranks", C.c_int),
+        ("topk_idx", C.c_void_p), ("topk_weights", C.c_void_p), ("num_topk", C.c_int),
+        ("num_experts", C.c_int), ("bias0", C.c_void_p), ("bias1", C.c_void_p),
+        ("out", C.c_void_p),
+    ]
+
+
 # name -> (restype, argtypes); mirrors include/ep_gb300.h
 _p, _i, _sz = C.c_void_p, C.c_int, C.c_size_t
 _LP = C.POINTER(ep_layout_t)
@@ -53,6 +76,9 @@ SIGNATURES = {
     "ep_get_layout_noalloc": (_i, [_p, _i, _i, _i, _i, _LP, _p]),
     "ep_dispatch": (_i, [_p, _i, _i, _p, _p, _i, _i, _i, _LP, _i, _p, _p, _p, _p, _p, _i, _p]),
     "ep_combine": (_i, [_p, _i, _i, _LP, _i, _i, _p, _p, _i, _i, _p, _p]),
+    "ep_fp8_packed_row_bytes": (_sz, [_i]),
+    "ep_dispatch_ex": (_i, [C.POINTER(ep_dispatch_args_t), _p]),
+    "ep_combine_ex": (_i, [C.POINTER(ep_combine_args_t), _p]),
     "ep_status_str": (C.c_char_p, [_i]),
     "ep_last_error": (C.c_char_p, []),
     "ep_abi_version": (_i, []),

@@ -146,100 +146,132 @@ ep_status_t ep_get_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t ep_fp8_packed_row_bytes(int hidden) {
+  if (hidden < EP_FP8_GROUP || hidden % EP_FP8_GROUP != 0 || hidden > EP_MAX_HIDDEN) return 0;
+  return fp8_packed_row_bytes(hidden);
+}
+
+ep_status_t ep_dispatch_ex(const ep_dispatch_args_t *args, ep_stream_t stream) {
+  static const char *fn = "ep_dispatch";
+  clear_error();
+  if (args == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: args is NULL", fn);
+  const ep_dispatch_args_t &x = *args;
+  if (x.num_tokens < 0) return fail(EP_ERR_INVALID_ARG, "%s: num_tokens=%d < 0", fn, x.num_tokens);
+  if (x.dtype != EP_DTYPE_BF16 && x.dtype != EP_DTYPE_FP8_E4M3 && x.dtype != EP_DTYPE_FP8_E4M3_PACKED)
+    return fail(EP_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)x.dtype);
+  const bool fp8 = x.dtype != EP_DTYPE_BF16;
+  const bool packed = x.dtype == EP_DTYPE_FP8_E4M3_PACKED;
+  if (x.hidden < 1) return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d < 1", fn, x.hidden);
+  if (x.hidden > EP_MAX_HIDDEN)
+    return fail(EP_ERR_UNSUPPORTED, "%s: hidden=%d > %d", fn, x.hidden, EP_MAX_HIDDEN);
+  if (x.hidden % (fp8 ? EP_FP8_GROUP : 8) != 0)
+    return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d is not a multiple of %d", fn, x.hidden,
+                fp8 ? EP_FP8_GROUP : 8);
+  EP_CHECK(check_routing_sizes(fn, x.num_topk, x.num_experts, x.num_ranks));
+  if (x.recv_capacity < 0) return fail(EP_ERR_INVALID_ARG, "%s: recv_capacity=%d < 0", fn, x.recv_capacity);
+  const bool any = x.num_tokens > 0;
+  const bool rows = x.recv_capacity > 0;
+  EP_CHECK(check_ptr(fn, "x", x.x, 16, any));
+  EP_CHECK(check_ptr(fn, "topk_idx", x.topk_idx, 8, any));
+  if (x.layout == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: layout is NULL", fn);
+  EP_CHECK(check_ptr(fn, "layout.token_slot", x.layout->token_slot, 4, any));
+  EP_CHECK(check_ptr(fn, "layout.error_word", x.layout->error_word, 4, true));
+  EP_CHECK(check_ptr(fn, "recv_x", x.recv_x, 16, rows));
+  EP_CHECK(check_ptr(fn, "recv_x_scales", x.recv_x_scales, 4, fp8 && !packed && rows));
+  EP_CHECK(check_ptr(fn, "recv_src_idx", x.recv_src_idx, 4, false));
+  EP_CHECK(check_ptr(fn, "recv_topk_idx", x.recv_topk_idx, 4, false));
+  EP_CHECK(check_ptr(fn, "recv_topk_weights", x.recv_topk_weights, 4, false));
+  EP_CHECK(check_ptr(fn, "topk_weights", x.topk_weights, 4, any && x.recv_topk_weights != nullptr));
+  EP_CHECK(check_ptr(fn, "cumulative_recv_stats", x.cumulative_recv_stats, 4, false));
+  DispatchArgs a;
+  a.x = static_cast<const uint16_t *>(x.x);
+  a.num_tokens = x.num_tokens;
+  a.hidden = x.hidden;
+  a.num_topk = x.num_topk;
+  a.num_experts = x.num_experts;
+  a.num_ranks = x.num_ranks;
+  a.topk_idx = x.topk_idx;
+  a.topk_weights = x.topk_weights;
+  a.token_slot = x.layout->token_slot;
+  a.error_word = x.layout->error_word;
+  a.fp8 = fp8;
+  a.packed_row_bytes = packed ? (int)fp8_packed_row_bytes(x.hidden) : 0;
+  a.recv_x = x.recv_x;
+  a.recv_x_scales = packed ? nullptr : x.recv_x_scales;
+  a.recv_src_idx = x.recv_src_idx;
+  a.recv_topk_idx = x.recv_topk_idx;
+  a.recv_topk_weights = x.recv_topk_weights;
+  a.recv_capacity = x.recv_capacity;
+  a.recv_stats = x.cumulative_recv_stats;
+  return launch_dispatch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 ep_status_t ep_dispatch(const void *x, int num_tokens, int hidden, const int64_t *topk_idx,
                         const float *topk_weights, int num_topk, int num_experts, int num_ranks,
                         const ep_layout_t *layout, ep_dtype_t dtype, void *recv_x, float *recv_x_scales,
                         int32_t *recv_src_idx, int32_t *recv_topk_idx, float *recv_topk_weights,
                         int recv_capacity, ep_stream_t stream) {
-  static const char *fn = "ep_dispatch";
+  const ep_dispatch_args_t a = {x,      num_tokens,   hidden,        topk_idx,      topk_weights,
+                                num_topk, num_experts, num_ranks,    layout,        dtype,
+                                recv_x, recv_x_scales, recv_src_idx, recv_topk_idx, recv_topk_weights,
+                                recv_capacity, nullptr};
+  return ep_dispatch_ex(&a, stream);
+}
+
+ep_status_t ep_combine_ex(const ep_combine_args_t *args, ep_stream_t stream) {
+  static const char *fn = "ep_combine";
   clear_error();
-  if (num_tokens < 0) return fail(EP_ERR_INVALID_ARG, "%s: num_tokens=%d < 0", fn, num_tokens);
-  if (dtype != EP_DTYPE_BF16 && dtype != EP_DTYPE_FP8_E4M3)
-    return fail(EP_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)dtype);
-  const bool fp8 = dtype == EP_DTYPE_FP8_E4M3;
-  if (hidden < 1) return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d < 1", fn, hidden);
-  if (hidden > EP_MAX_HIDDEN)
-    return fail(EP_ERR_UNSUPPORTED, "%s: hidden=%d > %d", fn, hidden, EP_MAX_HIDDEN);
-  if (hidden % (fp8 ? EP_FP8_GROUP : 8) != 0)
-    return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d is not a multiple of %d", fn, hidden, fp8 ? EP_FP8_GROUP : 8);
-  EP_CHECK(check_routing_sizes(fn, num_topk, num_experts, num_ranks));
-  if (recv_capacity < 0) return fail(EP_ERR_INVALID_ARG, "%s: recv_capacity=%d < 0", fn, recv_capacity);
-  const bool any = num_tokens > 0;
-  const bool rows = recv_capacity > 0;
-  EP_CHECK(check_ptr(fn, "x", x, 16, any));
-  EP_CHECK(check_ptr(fn, "topk_idx", topk_idx, 8, any));
-  if (layout == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: layout is NULL", fn);
-  EP_CHECK(check_ptr(fn, "layout.token_slot", layout->token_slot, 4, any));
-  EP_CHECK(check_ptr(fn, "layout.error_word", layout->error_word, 4, true));
-  EP_CHECK(check_ptr(fn, "recv_x", recv_x, 16, rows));
-  EP_CHECK(check_ptr(fn, "recv_x_scales", recv_x_scales, 4, fp8 && rows));
-  EP_CHECK(check_ptr(fn, "recv_src_idx", recv_src_idx, 4, false));
-  EP_CHECK(check_ptr(fn, "recv_topk_idx", recv_topk_idx, 4, false));
-  EP_CHECK(check_ptr(fn, "recv_topk_weights", recv_topk_weights, 4, false));
-  EP_CHECK(check_ptr(fn, "topk_weights", topk_weights, 4, any && recv_topk_weights != nullptr));
-  DispatchArgs a;
-  a.x = static_cast<const uint16_t *>(x);
-  a.num_tokens = num_tokens;
-  a.hidden = hidden;
-  a.num_topk = num_topk;
-  a.num_experts = num_experts;
-  a.num_ranks = num_ranks;
-  a.topk_idx = topk_idx;
-  a.topk_weights = topk_weights;
-  a.token_slot = layout->token_slot;
-  a.error_word = layout->error_word;
-  a.fp8 = fp8;
-  a.recv_x = recv_x;
-  a.recv_x_scales = recv_x_scales;
-  a.recv_src_idx = recv_src_idx;
-  a.recv_topk_idx = recv_topk_idx;
-  a.recv_topk_weights = recv_topk_weights;
-  a.recv_capacity = recv_capacity;
-  return launch_dispatch(a, reinterpret_cast<cudaStream_t>(stream));
+  if (args == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: args is NULL", fn);
+  const ep_combine_args_t &x = *args;
+  if (x.num_tokens < 0) return fail(EP_ERR_INVALID_ARG, "%s: num_tokens=%d < 0", fn, x.num_tokens);
+  if (x.recv_capacity < 0) return fail(EP_ERR_INVALID_ARG, "%s: recv_capacity=%d < 0", fn, x.recv_capacity);
+  if (x.hidden < 1) return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d < 1", fn, x.hidden);
+  if (x.hidden > EP_MAX_HIDDEN)
+    return fail(EP_ERR_UNSUPPORTED, "%s: hidden=%d > %d", fn, x.hidden, EP_MAX_HIDDEN);
+  if (x.hidden % 8 != 0) return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d is not a multiple of 8", fn, x.hidden);
+  if (x.num_ranks < 1 || x.num_ranks > EP_MAX_RANKS)
+    return fail(x.num_ranks < 1 ? EP_ERR_INVALID_ARG : EP_ERR_UNSUPPORTED, "%s: num_ranks=%d not in [1, %d]",
+                fn, x.num_ranks, EP_MAX_RANKS);
+  const bool weighted = x.topk_weights != nullptr;
+  if ((x.topk_idx == nullptr) != (x.topk_weights == nullptr))
+    return fail(EP_ERR_INVALID_ARG, "%s: topk_idx and topk_weights must both be given or both be NULL", fn);
+  const bool any = x.num_tokens > 0;
+  if (weighted) {
+    EP_CHECK(check_routing_sizes(fn, x.num_topk, x.num_experts, x.num_ranks));
+    EP_CHECK(check_ptr(fn, "topk_idx", x.topk_idx, 8, any));
+    EP_CHECK(check_ptr(fn, "topk_weights", x.topk_weights, 4, any));
+  }
+  EP_CHECK(check_ptr(fn, "y", x.y, 16, x.recv_capacity > 0 && any));
+  if (x.layout == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: layout is NULL", fn);
+  EP_CHECK(check_ptr(fn, "layout.token_slot", x.layout->token_slot, 4, any));
+  EP_CHECK(check_ptr(fn, "layout.error_word", x.layout->error_word, 4, true));
+  EP_CHECK(check_ptr(fn, "out", x.out, 16, any));
+  EP_CHECK(check_ptr(fn, "bias0", x.bias0, 16, false));
+  EP_CHECK(check_ptr(fn, "bias1", x.bias1, 16, false));
+  CombineArgs a;
+  a.y = static_cast<const uint16_t *>(x.y);
+  a.recv_capacity = x.recv_capacity;
+  a.hidden = x.hidden;
+  a.num_tokens = x.num_tokens;
+  a.num_ranks = x.num_ranks;
+  a.num_topk = weighted ? x.num_topk : 0;
+  a.num_experts = weighted ? x.num_experts : x.num_ranks;
+  a.token_slot = x.layout->token_slot;
+  a.error_word = x.layout->error_word;
+  a.topk_idx = x.topk_idx;
+  a.topk_weights = x.topk_weights;
+  a.bias0 = static_cast<const uint16_t *>(x.bias0);
+  a.bias1 = static_cast<const uint16_t *>(x.bias1);
+  a.out = static_cast<uint16_t *>(x.out);
+  return launch_combine(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 ep_status_t ep_combine(const void *y, int recv_capacity, int hidden, const ep_layout_t *layout,
                        int num_tokens, int num_ranks, const int64_t *topk_idx, const float *topk_weights,
                        int num_topk, int num_experts, void *out, ep_stream_t stream) {
-  static const char *fn = "ep_combine";
-  clear_error();
-  if (num_tokens < 0) return fail(EP_ERR_INVALID_ARG, "%s: num_tokens=%d < 0", fn, num_tokens);
-  if (recv_capacity < 0) return fail(EP_ERR_INVALID_ARG, "%s: recv_capacity=%d < 0", fn, recv_capacity);
-  if (hidden < 1) return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d < 1", fn, hidden);
-  if (hidden > EP_MAX_HIDDEN)
-    return fail(EP_ERR_UNSUPPORTED, "%s: hidden=%d > %d", fn, hidden, EP_MAX_HIDDEN);
-  if (hidden % 8 != 0) return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d is not a multiple of 8", fn, hidden);
-  if (num_ranks < 1 || num_ranks > EP_MAX_RANKS)
-    return fail(num_ranks < 1 ? EP_ERR_INVALID_ARG : EP_ERR_UNSUPPORTED, "%s: num_ranks=%d not in [1, %d]",
-                fn, num_ranks, EP_MAX_RANKS);
-  const bool weighted = topk_weights != nullptr;
-  if ((topk_idx == nullptr) != (topk_weights == nullptr))
-    return fail(EP_ERR_INVALID_ARG, "%s: topk_idx and topk_weights must both be given or both be NULL", fn);
-  const bool any = num_tokens > 0;
-  if (weighted) {
-    EP_CHECK(check_routing_sizes(fn, num_topk, num_experts, num_ranks));
-    EP_CHECK(check_ptr(fn, "topk_idx", topk_idx, 8, any));
-    EP_CHECK(check_ptr(fn, "topk_weights", topk_weights, 4, any));
-  }
-  EP_CHECK(check_ptr(fn, "y", y, 16, recv_capacity > 0 && any));
-  if (layout == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: layout is NULL", fn);
-  EP_CHECK(check_ptr(fn, "layout.token_slot", layout->token_slot, 4, any));
-  EP_CHECK(check_ptr(fn, "layout.error_word", layout->error_word, 4, true));
-  EP_CHECK(check_ptr(fn, "out", out, 16, any));
-  CombineArgs a;
-  a.y = static_cast<const uint16_t *>(y);
-  a.recv_capacity = recv_capacity;
-  a.hidden = hidden;
-  a.num_tokens = num_tokens;
-  a.num_ranks = num_ranks;
-  a.num_topk = weighted ? num_topk : 0;
-  a.num_experts = weighted ? num_experts : num_ranks;
-  a.token_slot = layout->token_slot;
-  a.error_word = layout->error_word;
-  a.topk_idx = topk_idx;
-  a.topk_weights = topk_weights;
-  a.out = static_cast<uint16_t *>(out);
-  return launch_combine(a, reinterpret_cast<cudaStream_t>(stream));
+  const ep_combine_args_t a = {y,        recv_capacity, hidden,       layout,  num_tokens, num_ranks, topk_idx,
+                               topk_weights, num_topk,  num_experts,  nullptr, nullptr,    out};
+  return ep_combine_ex(&a, stream);
 }
 
 const char *ep_status_str(ep_status_t status) {

@@ -33,8 +33,24 @@ struct CombineParams {
   uint32_t *error_word;
   const int64_t *topk_idx;
   const float *topk_weights;
+  const uint16_t *bias0, *bias1;  // [T*H] or null: seed the accumulator
   uint16_t *out;
 };
+
+// acc = bias0 (or 0), then acc = acc + bias1, for 8 consecutive elements.
+__device__ __forceinline__ void seed(float (&acc)[8], const CombineParams &p, int4 b0, int4 b1) {
+  const uint32_t w0[4] = {(uint32_t)b0.x, (uint32_t)b0.y, (uint32_t)b0.z, (uint32_t)b0.w};
+  const uint32_t w1[4] = {(uint32_t)b1.x, (uint32_t)b1.y, (uint32_t)b1.z, (uint32_t)b1.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    acc[2 * q] = p.bias0 != nullptr ? bf16_lo(w0[q]) : 0.0f;
+    acc[2 * q + 1] = p.bias0 != nullptr ? bf16_hi(w0[q]) : 0.0f;
+    if (p.bias1 != nullptr) {
+      acc[2 * q] = __fadd_rn(acc[2 * q], bf16_lo(w1[q]));
+      acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], bf16_hi(w1[q]));
+    }
+  }
+}
 
 template <bool WEIGHTED>
 __device__ __forceinline__ void accumulate(float (&acc)[8], int4 v, float c) {
@@ -115,9 +131,13 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
     for (int col0 = tid; col0 < ncol; col0 += kCombineThreads * kCombineCols) {
       float acc[kCombineCols][8];
 #pragma unroll
-      for (int c = 0; c < kCombineCols; ++c)
-#pragma unroll
-        for (int q = 0; q < 8; ++q) acc[c][q] = 0.0f;
+      for (int c = 0; c < kCombineCols; ++c) {
+        const int col = col0 + c * kCombineThreads;
+        const bool in = col < ncol;
+        const int4 z = make_int4(0, 0, 0, 0);
+        seed(acc[c], p, (in && p.bias0) ? ld_stream_v4(p.bias0 + (size_t)t * p.H + (size_t)col * 8) : z,
+             (in && p.bias1) ? ld_stream_v4(p.bias1 + (size_t)t * p.H + (size_t)col * 8) : z);
+      }
       for (int j0 = 0; j0 < n; j0 += kRowsPerBatch) {
         int4 v[kCombineCols][kRowsPerBatch];
 #pragma unroll
@@ -286,6 +306,12 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
         const int s = static_cast<int>(i % kCombineStages);
         const int cols = min(kChunk, p.H - c * kChunk) / 8;
         const unsigned char *stage = stages + (size_t)s * kStageBytes;
+        // a unit has at most one column per reducer thread: its bias loads
+        // are issued before the wait for the rows
+        const size_t bcol = (size_t)t * p.H + (size_t)c * kChunk + (size_t)rt * 8;
+        const int4 z = make_int4(0, 0, 0, 0);
+        const int4 b0 = (rt < cols && p.bias0) ? ld_stream_v4(p.bias0 + bcol) : z;
+        const int4 b1 = (rt < cols && p.bias1) ? ld_stream_v4(p.bias1 + bcol) : z;
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (uint32_t)(i / kCombineStages) & 1u))) {
           if (lane == 0) {
             *s_abort = 1;
@@ -297,10 +323,11 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
         const int nrows = *reinterpret_cast<const int *>(stage);
         const float *hdr_coef = reinterpret_cast<const float *>(stage + 16);
         uint16_t *out = p.out + (size_t)t * p.H + (size_t)c * kChunk;
-        for (int col = rt; col < cols; col += kReducers * kWarpSize) {
+        static_assert(kChunk / 8 <= kReducers * kWarpSize, "one column per reducer thread");
+        if (rt < cols) {
+          const int col = rt;
           float acc[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+          seed(acc, p, b0, b1);
           for (int r = 0; r < nrows; ++r) {
             const int4 v =
                 *reinterpret_cast<const int4 *>(stage + kStageHeader + (size_t)r * kChunkBytes + col * 16);
@@ -388,6 +415,8 @@ ep_status_t launch_combine(const CombineArgs &a, cudaStream_t stream) {
   p.error_word = a.error_word;
   p.topk_idx = a.topk_idx;
   p.topk_weights = a.topk_weights;
+  p.bias0 = a.bias0;
+  p.bias1 = a.bias1;
   p.out = a.out;
   const bool weighted = a.topk_weights != nullptr;
   if (kUseWsCombine && a.num_ranks <= kWsMaxRanks)

@@ -47,9 +47,11 @@ struct DispatchParams {
   int32_t *recv_topk_idx;
   float *recv_topk_weights;
   int cap;
+  uint32_t *stats;         // [E] cumulative received (row, top-k slot) counts, or null
   int stages;
   uint32_t row_in_bytes;   // 2H
-  uint32_t row_out_bytes;  // 2H (bf16) or H (fp8)
+  uint32_t row_out_bytes;  // 2H (bf16), H (fp8) or the packed fp8 row
+  bool packed;             // fp8 codes, scales and zero padding in one row
   uint32_t stage_stride;   // row_in_bytes rounded up to 128
   uint32_t out_stride;     // fp8 output row, H rounded up to 128
   uint32_t scale_stride;   // fp8 scales of one row, groups*4 rounded up to 16
@@ -62,6 +64,18 @@ __device__ __forceinline__ void issue_row_load(const DispatchParams &p, unsigned
   mbar_arrive_expect_tx(&full[s], p.row_in_bytes);
   bulk_load_hint(stages + (size_t)s * p.stage_stride, p.x + (size_t)t * p.H, p.row_in_bytes,
                  &full[s], policy);
+}
+
+// Cumulative recv stats: lane k < K adds one to its expert's count when the
+// row of the expert's rank was received (slot in [0, cap)).  Warp-collective.
+__device__ __forceinline__ void count_received(const DispatchParams &p, int64_t e, int slot_lo, int slot_hi,
+                                               int lane) {
+  const bool valid = e >= 0 && e < p.E;
+  const int r = valid ? static_cast<int>(e) / p.epr : 0;
+  const int s_lo = __shfl_sync(0xffffffffu, slot_lo, r & (kWarpSize - 1));
+  const int s_hi = __shfl_sync(0xffffffffu, slot_hi, r & (kWarpSize - 1));
+  const int slot = r < kWarpSize ? s_lo : s_hi;
+  if (valid && slot >= 0 && slot < p.cap) atomicAdd(p.stats + e, 1u);
 }
 
 // Received metadata of token t, by threads [32, blockDim): source token,
@@ -79,6 +93,7 @@ __device__ __forceinline__ void write_metadata(const DispatchParams &p, int t,
     const int hi = lane + kWarpSize < p.R ? slots[lane + kWarpSize] : -1;
     if (!ranks_agree(e, p.E, p.epr, p.R, lo, hi, lane) && lane == 0)
       set_error(p.error_word, EP_ERRBIT_STALE_LAYOUT);
+    if (p.stats != nullptr) count_received(p, e, lo, hi, lane);
   }
   if (p.recv_src_idx != nullptr) {
     for (int j = mt; j < p.R; j += nt) {
@@ -301,6 +316,12 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
     *s_abort = 0;
     fence_barrier_init();
   }
+  if (p.packed) {  // the padding of both packed output rows stays zero
+    const uint32_t used = (uint32_t)p.H + (uint32_t)p.groups * 4u;
+    for (int o = 0; o < kWsOut; ++o)
+      for (uint32_t b = used + tid; b < p.row_out_bytes; b += kWsThreads) out[(size_t)o * p.out_stride + b] = 0;
+    fence_proxy_async_smem();
+  }
   __syncthreads();
   griddep_wait();
   griddep_launch_dependents();
@@ -343,6 +364,7 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
         set_error(p.error_word, EP_ERRBIT_CAPACITY);
         slot_hi = -1;
       }
+      if (p.stats != nullptr) count_received(p, e, slot_lo, slot_hi, lane);
       const float w = (lane < p.K && p.recv_topk_weights != nullptr)
                           ? __ldg(p.topk_weights + (size_t)t * p.K + lane) : 0.0f;
       // received metadata: needs no shared memory, runs ahead of the cast
@@ -367,6 +389,19 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
       }
       const unsigned char *orow = out + (size_t)o * p.out_stride;
       const float *oscale = osc + (size_t)o * (p.scale_stride / 4);
+      if (p.packed) {  // codes, scales and padding go out as one row
+        if (slot_lo >= 0)
+          bulk_store(static_cast<unsigned char *>(p.recv_x) + (size_t)slot_lo * p.row_out_bytes, orow,
+                     p.row_out_bytes);
+        if (slot_hi >= 0)
+          bulk_store(static_cast<unsigned char *>(p.recv_x) + (size_t)slot_hi * p.row_out_bytes, orow,
+                     p.row_out_bytes);
+        bulk_commit();
+        bulk_wait_read<0>();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_out[o]);
+        continue;
+      }
       if (slot_lo >= 0) {
         bulk_store(static_cast<unsigned char *>(p.recv_x) + (size_t)slot_lo * p.H, orow, p.row_out_bytes);
         if (scale_bulk) bulk_store(p.recv_x_scales + (size_t)slot_lo * p.groups, oscale, p.scale_stride);
@@ -409,7 +444,7 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
       }
       const unsigned char *stage = in + (size_t)s * p.stage_stride;
       unsigned char *orow = out + (size_t)o * p.out_stride;
-      float *oscale = osc + (size_t)o * (p.scale_stride / 4);
+      float *oscale = p.packed ? reinterpret_cast<float *>(orow + p.H) : osc + (size_t)o * (p.scale_stride / 4);
       for (int g = cw; g < p.groups; g += kWsCasters) {
         float scale;
         const uint2 raw = *reinterpret_cast<const uint2 *>(stage + (size_t)g * 256 + lane * 8);
@@ -528,12 +563,15 @@ ep_status_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream) {
   p.recv_topk_idx = a.recv_topk_idx;
   p.recv_topk_weights = a.recv_topk_weights;
   p.cap = a.recv_capacity;
+  p.stats = a.recv_stats;
+  p.packed = a.packed_row_bytes > 0;
   p.row_in_bytes = 2u * (uint32_t)a.hidden;
-  p.row_out_bytes = a.fp8 ? (uint32_t)a.hidden : 2u * (uint32_t)a.hidden;
+  p.row_out_bytes = p.packed ? (uint32_t)a.packed_row_bytes : a.fp8 ? (uint32_t)a.hidden : 2u * (uint32_t)a.hidden;
   p.stage_stride = (p.row_in_bytes + 127u) / 128u * 128u;
-  p.out_stride = a.fp8 ? ((uint32_t)a.hidden + 127u) / 128u * 128u : 0u;
-  p.scale_stride = a.fp8 ? ((uint32_t)p.groups * 4u + 15u) / 16u * 16u : 0u;
-  if (a.fp8) return kFp8WarpSpecialised ? launch_ws(p, *di, stream) : launch_ring<true>(p, *di, stream);
+  p.out_stride = a.fp8 ? (p.row_out_bytes + 127u) / 128u * 128u : 0u;
+  p.scale_stride = (a.fp8 && !p.packed) ? ((uint32_t)p.groups * 4u + 15u) / 16u * 16u : 0u;
+  // packed rows are only built by the warp-specialised kernel
+  if (a.fp8) return (kFp8WarpSpecialised || p.packed) ? launch_ws(p, *di, stream) : launch_ring<true>(p, *di, stream);
   return launch_ring<false>(p, *di, stream);
 }
 

@@ -39,6 +39,15 @@ ep_status_t launch_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
                           cudaStream_t stream);
 
 // ---- dispatch (ep_dispatch.cu)
+// Bytes of a packed fp8 row: codes, scales, zero padding to 16 bytes, or to
+// 512 when that adds under 5% to the unpadded row.
+inline size_t fp8_packed_row_bytes(int hidden) {
+  const size_t raw = (size_t)hidden + (size_t)(hidden / EP_FP8_GROUP) * 4;
+  const size_t pad16 = (raw + 15) / 16 * 16;
+  const size_t pad512 = (raw + 511) / 512 * 512;
+  return (pad512 - raw) * 20 < raw ? pad512 : pad16;
+}
+
 struct DispatchArgs {
   const uint16_t *x;
   int num_tokens, hidden, num_topk, num_experts, num_ranks;
@@ -47,12 +56,14 @@ struct DispatchArgs {
   const int32_t *token_slot;
   uint32_t *error_word;
   bool fp8;
+  int packed_row_bytes;  // > 0: packed fp8 rows of this many bytes
   void *recv_x;
   float *recv_x_scales;
   int32_t *recv_src_idx;
   int32_t *recv_topk_idx;
   float *recv_topk_weights;
   int recv_capacity;
+  uint32_t *recv_stats;  // [E] or null
 };
 ep_status_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream);
 
@@ -64,6 +75,7 @@ struct CombineArgs {
   uint32_t *error_word;
   const int64_t *topk_idx;
   const float *topk_weights;
+  const uint16_t *bias0, *bias1;  // [T*H] or null
   uint16_t *out;
 };
 ep_status_t launch_combine(const CombineArgs &a, cudaStream_t stream);

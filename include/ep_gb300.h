@@ -55,8 +55,10 @@ typedef enum {
 } ep_status_t;
 
 typedef enum {
-    EP_DTYPE_BF16 = 0,       /* received rows are bit copies of x          */
-    EP_DTYPE_FP8_E4M3 = 1    /* received rows are e4m3 codes + fp32 scales */
+    EP_DTYPE_BF16 = 0,          /* received rows are bit copies of x          */
+    EP_DTYPE_FP8_E4M3 = 1,      /* e4m3 rows + a separate fp32 scale array    */
+    EP_DTYPE_FP8_E4M3_PACKED = 2 /* e4m3 codes, fp32 scales and zero padding
+                                    in one row of ep_fp8_packed_row_bytes(H) */
 } ep_dtype_t;
 
 /* Bits of the device error word (ep_layout_t.error_word). */
@@ -220,6 +222,49 @@ ep_status_t ep_dispatch(const void *x, int num_tokens, int hidden,
                         ep_stream_t stream);
 
 /*
+ * Bytes of one packed fp8 row (EP_DTYPE_FP8_E4M3_PACKED): the H e4m3 codes,
+ * then the H/128 fp32 scales, then zero padding to a multiple of 16 bytes,
+ * or of 512 bytes when that padding adds under 5% to the unpadded row
+ * (TileScale PR #68, commit message on packing the fp8 row: 132 raw bytes at
+ * hidden 128; 7392 raw, 7680 padded at 7168).  0 if hidden is not a
+ * positive multiple of 128.
+ */
+size_t ep_fp8_packed_row_bytes(int hidden);
+
+/*
+ * Dispatch with every option.  Members as for ep_dispatch, plus:
+ *   dtype == EP_DTYPE_FP8_E4M3_PACKED: recv_x is uint8
+ *     [recv_capacity * ep_fp8_packed_row_bytes(H)]; each row holds the codes,
+ *     then the scales, then zeros (TileScale PR #68, commit message on packing
+ *     the fp8 row); recv_x_scales is ignored.  H % 128 == 0.
+ *   cumulative_recv_stats  uint32 [E] or NULL: for every received
+ *     (row, top-k slot) of expert e, stats[e] += 1 -- rank r's count for its
+ *     local expert e - r*E/R, accumulated, never cleared, so the caller picks
+ *     the window by zeroing it (same page, commit message adding cumulative
+ *     recv stats).
+ */
+typedef struct {
+    const void *x;
+    int num_tokens;
+    int hidden;
+    const int64_t *topk_idx;
+    const float *topk_weights;
+    int num_topk;
+    int num_experts;
+    int num_ranks;
+    const ep_layout_t *layout;
+    ep_dtype_t dtype;
+    void *recv_x;
+    float *recv_x_scales;
+    int32_t *recv_src_idx;
+    int32_t *recv_topk_idx;
+    float *recv_topk_weights;
+    int recv_capacity;
+    uint32_t *cumulative_recv_stats;
+} ep_dispatch_args_t;
+ep_status_t ep_dispatch_ex(const ep_dispatch_args_t *args, ep_stream_t stream);
+
+/*
  * Combine: the local reduce of TileScale PR #68 (PR summary: one block per
  * source token reduces the rows stored back for it).  On one GPU the
  * store-back slot comm_x[rank][src_token] is the received row
@@ -249,6 +294,31 @@ ep_status_t ep_combine(const void *y, int recv_capacity, int hidden,
                        const int64_t *topk_idx, const float *topk_weights,
                        int num_topk, int num_experts, void *out,
                        ep_stream_t stream);
+
+/*
+ * Combine with every option.  Members as for ep_combine, plus:
+ *   bias0, bias1  bf16 [T*H] or NULL, 16-byte aligned: they seed the fp32
+ *     accumulator, acc = bias0 (or 0), then acc = acc + bias1, before the
+ *     rank rows are added, so a token sent nowhere comes back as its bias
+ *     (TileScale PR #68, commit message adding combine bias: bias_0/bias_1
+ *     seed the reduce accumulator).
+ */
+typedef struct {
+    const void *y;
+    int recv_capacity;
+    int hidden;
+    const ep_layout_t *layout;
+    int num_tokens;
+    int num_ranks;
+    const int64_t *topk_idx;
+    const float *topk_weights;
+    int num_topk;
+    int num_experts;
+    const void *bias0;
+    const void *bias1;
+    void *out;
+} ep_combine_args_t;
+ep_status_t ep_combine_ex(const ep_combine_args_t *args, ep_stream_t stream);
 
 /* A static, human-readable name of a status. */
 const char *ep_status_str(ep_status_t status);

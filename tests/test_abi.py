@@ -152,3 +152,44 @@ def test_status_strings(lib):
     assert [lib.ep_status_str(i).decode() for i in range(4)] == [
         "EP_OK", "EP_ERR_INVALID_ARG", "EP_ERR_UNSUPPORTED", "EP_ERR_CUDA"]
     assert lib.ep_abi_version() == 1
+
+
+def test_packed_row_bytes_matches_oracle(lib):
+    import oracle
+    for H in list(range(128, 16385, 128)):
+        assert lib.ep_fp8_packed_row_bytes(H) == oracle.fp8_packed_row_bytes(H), H
+    assert lib.ep_fp8_packed_row_bytes(100) == 0 and lib.ep_fp8_packed_row_bytes(0) == 0
+
+
+def _dargs(**kw):
+    from combine_ep_get_layout_gb300 import _native as N
+    lay = _layout()
+    a = dict(x=0x20000, num_tokens=100, hidden=256, topk_idx=0x20000, topk_weights=0x20000,
+             num_topk=4, num_experts=16, num_ranks=4, layout=C.pointer(lay), dtype=0,
+             recv_x=0x20000, recv_x_scales=0x20000, recv_src_idx=None, recv_topk_idx=None,
+             recv_topk_weights=None, recv_capacity=400, cumulative_recv_stats=None)
+    a.update(kw)
+    return N.ep_dispatch_args_t(**a), lay
+
+
+@pytest.mark.parametrize("kw,needle", [
+    (dict(dtype=2, hidden=264), "multiple of 128"),
+    (dict(cumulative_recv_stats=0x20002), "cumulative_recv_stats is not 4-byte aligned"),
+    (dict(dtype=9), "dtype"),
+])
+def test_dispatch_ex_rejects(lib, kw, needle):
+    a, _keep = _dargs(**kw)
+    s = lib.ep_dispatch_ex(C.byref(a), None)
+    name, msg = _status(lib, s)
+    assert name == "EP_ERR_INVALID_ARG", (name, msg)
+    assert needle in msg
+    assert _status(lib, lib.ep_dispatch_ex(None, None))[0] == "EP_ERR_INVALID_ARG"
+
+
+def test_combine_ex_rejects_misaligned_bias(lib):
+    from combine_ep_get_layout_gb300 import _native as N
+    lay = _layout()
+    a = N.ep_combine_args_t(0x20000, 400, 256, C.pointer(lay), 100, 4, 0x20000, 0x20000, 4, 16,
+                            0x20008, None, 0x20000)
+    name, msg = _status(lib, lib.ep_combine_ex(C.byref(a), None))
+    assert name == "EP_ERR_INVALID_ARG" and "bias0" in msg
