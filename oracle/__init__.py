@@ -30,6 +30,7 @@ _LIB = os.path.join(_HERE, "libep_oracle.so")
 BAD_INDEX = 1
 CAPACITY = 2
 STALE = 8
+DUP = 16
 
 _lock = threading.Lock()
 _default = None
@@ -78,6 +79,12 @@ def _bind(path: str):
     L.ora_combine_ex.restype = i
     L.ora_fp8_packed_row_bytes.argtypes = [i]
     L.ora_fp8_packed_row_bytes.restype = i
+    L.ora_get_layout_expanded.argtypes = [p, i, i, i, i, p, p, p]
+    L.ora_get_layout_expanded.restype = i
+    L.ora_dispatch_expanded.argtypes = [p, i, i, p, p, i, i, i, p, p, p, i, i, p, p, p, p, p, i, p]
+    L.ora_dispatch_expanded.restype = i
+    L.ora_combine_expanded.argtypes = [p, i, i, p, i, i, p, p, i, p, p, p]
+    L.ora_combine_expanded.restype = i
     return L
 
 
@@ -222,6 +229,66 @@ class Oracle:
                                      _ptr(b0), _ptr(b1), _ptr(out))
         return out, int(err)
 
+    # ------------------------------------------------------ expanded layout
+
+    def get_layout_expanded(self, topk_idx, num_experts: int, expert_alignment: int = 1) -> dict:
+        idx = _c(topk_idx, np.int64)
+        T, K = idx.shape
+        E = num_experts
+        out = {"num_rows_per_expert": np.empty(E, np.int32),
+               "expert_offset": np.empty(E + 1, np.int32),
+               "token_slot": np.empty((T, K), np.int32)}
+        err = self._L.ora_get_layout_expanded(
+            _ptr(idx), T, K, E, int(expert_alignment), _ptr(out["num_rows_per_expert"]),
+            _ptr(out["expert_offset"]), _ptr(out["token_slot"]))
+        out["error"] = int(err)
+        return out
+
+    def dispatch_expanded(self, x_bits, topk_idx, topk_weights, num_experts: int,
+                          num_ranks: int, layout: dict, fp8, recv_capacity: int,
+                          zero_padding: bool = True, stats=None) -> dict:
+        mode = 2 if fp8 == "packed" else (1 if fp8 else 0)
+        x = _c(x_bits, np.uint16)
+        idx = _c(topk_idx, np.int64)
+        w = _c(topk_weights, np.float32)
+        T, H = x.shape
+        K = idx.shape[1]
+        cap = int(recv_capacity)
+        G = H // 128
+        width = H if mode < 2 else self.fp8_packed_row_bytes(H)
+        recv_x = np.full((cap + 1, width), 0x5a if mode else 0x5a5a, np.uint8 if mode else np.uint16)
+        scales = np.full((cap + 1, G), 7.0, np.float32) if mode == 1 else None
+        src = np.full(cap + 1, -7, np.int32)
+        ridx = np.full((cap + 1, K), -7, np.int32)
+        rw = np.full((cap + 1, K), np.nan, np.float32)
+        err = self._L.ora_dispatch_expanded(
+            _ptr(x), T, H, _ptr(idx), _ptr(w), K, num_experts, num_ranks,
+            _ptr(_c(layout["token_slot"], np.int32)), _ptr(_c(layout["expert_offset"], np.int32)),
+            _ptr(_c(layout["num_rows_per_expert"], np.int32)), mode, 1 if zero_padding else 0,
+            _ptr(recv_x), _ptr(scales), _ptr(src), _ptr(ridx), _ptr(rw), cap, _ptr(stats))
+        if src[cap] != -7 or np.any(ridx[cap] != -7):
+            raise AssertionError("dispatch wrote past its capacity")
+        return {"recv_x": recv_x[:cap],
+                "recv_x_scales": None if scales is None else scales[:cap],
+                "recv_src_idx": src[:cap], "recv_topk_idx": ridx[:cap],
+                "recv_topk_weights": rw[:cap], "error": int(err)}
+
+    def combine_expanded(self, y_bits, token_slot, topk_idx=None, topk_weights=None,
+                         num_experts: int = 0, bias0=None, bias1=None):
+        y = _c(y_bits, np.uint16)
+        slot = _c(token_slot, np.int32)
+        cap, H = y.shape
+        T, K = slot.shape
+        weighted = topk_weights is not None
+        idx = _c(topk_idx, np.int64) if weighted else None
+        w = _c(topk_weights, np.float32) if weighted else None
+        b0 = None if bias0 is None else _c(bias0, np.uint16)
+        b1 = None if bias1 is None else _c(bias1, np.uint16)
+        out = np.empty((T, H), np.uint16)
+        err = self._L.ora_combine_expanded(_ptr(y), cap, H, _ptr(slot), T, K, _ptr(idx),
+                                           _ptr(w), num_experts, _ptr(b0), _ptr(b1), _ptr(out))
+        return out, int(err)
+
     def run_path(self, inputs: dict, num_experts: int, num_ranks: int,
                  fp8: bool, recv_capacity: int, y_bits=None,
                  weighted: bool = True) -> dict:
@@ -259,5 +326,6 @@ def _forward(name):
 
 for _n in ("bf16_to_f32", "f32_to_bf16", "e4m3_to_f64", "f32_to_e4m3",
            "quantize_row", "fp8_packed_row_bytes", "get_layout", "dispatch",
-           "combine", "run_path"):
+           "combine", "get_layout_expanded", "dispatch_expanded", "combine_expanded",
+           "run_path"):
     globals()[_n] = _forward(_n)

@@ -34,6 +34,11 @@
  *   [TS-BIAS]   same page, commit message adding combine bias and cumulative
  *               recv stats: bias_0/bias_1 seed the reduce accumulator; the
  *               stats accumulate each local expert's received count.
+ *   [TS-EXPAND] (also) one received row per (token, expert) instead of per
+ *               (token, rank), grouped by local expert, each segment rounded
+ *               up to expert_alignment rows, zero_padding clearing the gap;
+ *               an expanded row marks only the expert it belongs to; the
+ *               expanded combine sums a token's rows (kDoExpandedSend).
  *   [TS-CACHE]  same page, commit messages on the cached-layout dispatch
  *               (handle=): a layout depends only on the routing; a stale one
  *               misroutes silently, so it is guarded.
@@ -49,6 +54,13 @@
  *   - packed row: the 5% is the padding of the 512-byte form relative to the
  *     unpadded row (the page's +3.9% at hidden 7168, +21% at 2048, +9% at
  *     4096); padding bytes are zero.
+ *   - expanded layout: rows are expert-major (rank-major, then local
+ *     expert); inside an expert's segment in ascending (token, k) order;
+ *     a token naming an expert a second time gets no second row (flag
+ *     EP_ORA_DUP); padding rows, when zero_padding is asked for, hold zeros
+ *     and are marked unoccupied (source -1, every top-k slot -1, weight 0);
+ *     the expanded combine adds a token's rows in ascending row order, each
+ *     times its own gate weight (or 1), in fp32 after the biases.
  *   - stale layout: dispatch and weighted combine flag EP_ORA_STALE for a
  *     token whose set of ranks under the routing they are given differs
  *     from the ranks with a slot in the layout (the slots depend on nothing
@@ -73,6 +85,7 @@
 #define EP_ORA_BAD_INDEX 1
 #define EP_ORA_CAPACITY 2
 #define EP_ORA_STALE 8      /* routing and layout disagree on a token's ranks */
+#define EP_ORA_DUP 16       /* expanded layout: a token names an expert twice */
 
 /* ------------------------------------------------------------------ */
 /* Number formats                                                      */
@@ -450,4 +463,219 @@ void ora_f32_to_bf16_array(const float *x, long n, uint16_t *b)
 {
     for (long i = 0; i < n; ++i)
         b[i] = ora_f32_to_bf16(x[i]);
+}
+
+
+/* ------------------------------------------------------------------ */
+/* Expanded layout: one row per (token, expert), grouped by expert      */
+/* ------------------------------------------------------------------ */
+
+/* 1 if topk_idx[t][k] is a valid expert not named at an earlier k of t. */
+static int first_choice(const int64_t *topk_idx, int t, int k, int K, int E)
+{
+    int64_t e = topk_idx[(size_t)t * K + k];
+    if (!valid_expert(e, E))
+        return 0;
+    for (int j = 0; j < k; ++j)
+        if (topk_idx[(size_t)t * K + j] == e)
+            return 0;
+    return 1;
+}
+
+/*
+ * Outputs: num_rows_per_expert [E] (rows, one per first choice),
+ * expert_offset [E+1] (aligned exclusive prefix; [E] = rows incl. padding),
+ * token_slot [T*K] (row of (t, k), -1 where none).  Returns error bits.
+ */
+int ora_get_layout_expanded(const int64_t *topk_idx, int T, int K, int E,
+                            int align, int32_t *num_rows_per_expert,
+                            int32_t *expert_offset, int32_t *token_slot)
+{
+    int err = 0;
+    memset(num_rows_per_expert, 0, sizeof(int32_t) * (size_t)E);
+    for (int t = 0; t < T; ++t) {
+        for (int k = 0; k < K; ++k) {
+            int64_t e = topk_idx[(size_t)t * K + k];
+            if (e == -1)
+                continue;
+            if (!valid_expert(e, E)) {
+                err |= EP_ORA_BAD_INDEX;
+                continue;
+            }
+            if (!first_choice(topk_idx, t, k, K, E)) {
+                err |= EP_ORA_DUP;
+                continue;
+            }
+            num_rows_per_expert[e] += 1;
+        }
+    }
+    expert_offset[0] = 0;
+    for (int e = 0; e < E; ++e) {
+        int rows = num_rows_per_expert[e];
+        int aligned = (rows + align - 1) / align * align;
+        expert_offset[e + 1] = expert_offset[e] + aligned;
+    }
+    int32_t *next = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E > 0 ? E : 1));
+    for (int e = 0; e < E; ++e)
+        next[e] = expert_offset[e];
+    for (int t = 0; t < T; ++t)
+        for (int k = 0; k < K; ++k)
+            token_slot[(size_t)t * K + k] =
+                first_choice(topk_idx, t, k, K, E)
+                    ? next[topk_idx[(size_t)t * K + k]]++ : -1;
+    free(next);
+    return err;
+}
+
+/* Whether the expanded layout's slots of token t match its first choices. */
+static int choices_agree(const int64_t *topk_idx, int t, int K, int E,
+                         const int32_t *token_slot)
+{
+    for (int k = 0; k < K; ++k)
+        if (first_choice(topk_idx, t, k, K, E) != (token_slot[(size_t)t * K + k] >= 0))
+            return 0;
+    return 1;
+}
+
+/*
+ * Expanded dispatch.  fp8 as in ora_dispatch_ex (0 bf16, 1 fp8 + scales,
+ * 2 packed).  Padding rows of each expert's segment are written only when
+ * zero_padding != 0.  Rows with slot >= cap are skipped (EP_ORA_CAPACITY).
+ */
+int ora_dispatch_expanded(const uint16_t *x, int T, int H, const int64_t *topk_idx,
+                          const float *topk_weights, int K, int E, int R,
+                          const int32_t *token_slot, const int32_t *expert_offset,
+                          const int32_t *num_rows_per_expert, int fp8,
+                          int zero_padding, void *recv_x, float *recv_x_scales,
+                          int32_t *recv_src_idx, int32_t *recv_topk_idx,
+                          float *recv_topk_weights, int cap, uint32_t *stats)
+{
+    int err = 0;
+    int epr = E / R;
+    int G = H / 128;
+    size_t width = fp8 == 2 ? (size_t)ora_fp8_packed_row_bytes(H)
+                            : (size_t)H * (fp8 ? 1 : 2);
+    uint8_t *q = (uint8_t *)malloc((size_t)(H > 0 ? H : 1));
+    float *sc = (float *)malloc(sizeof(float) * (size_t)(G > 0 ? G : 1));
+    for (int t = 0; t < T; ++t) {
+        const uint16_t *row = x + (size_t)t * H;
+        if (!choices_agree(topk_idx, t, K, E, token_slot))
+            err |= EP_ORA_STALE;
+        if (fp8)
+            ora_quantize_row(row, H, q, sc);
+        for (int k = 0; k < K; ++k) {
+            int32_t slot = token_slot[(size_t)t * K + k];
+            if (slot < 0)
+                continue;
+            if (slot >= cap) {
+                err |= EP_ORA_CAPACITY;
+                continue;
+            }
+            int64_t e = topk_idx[(size_t)t * K + k];
+            uint8_t *dst = (uint8_t *)recv_x + (size_t)slot * width;
+            if (!fp8) {
+                memcpy(dst, row, sizeof(uint16_t) * (size_t)H);
+            } else if (fp8 == 1) {
+                memcpy(dst, q, (size_t)H);
+                memcpy(recv_x_scales + (size_t)slot * G, sc, sizeof(float) * (size_t)G);
+            } else {
+                memset(dst, 0, width);
+                memcpy(dst, q, (size_t)H);
+                memcpy(dst + H, sc, sizeof(float) * (size_t)G);
+            }
+            if (recv_src_idx)
+                recv_src_idx[slot] = t;
+            for (int j = 0; j < K; ++j) {
+                /* an expanded row marks only the expert it belongs to */
+                int here = j == k && valid_expert(e, E);
+                if (recv_topk_idx)
+                    recv_topk_idx[(size_t)slot * K + j] =
+                        here ? (int32_t)(e - (e / epr) * epr) : -1;
+                if (recv_topk_weights)
+                    recv_topk_weights[(size_t)slot * K + j] =
+                        here ? topk_weights[(size_t)t * K + k] : 0.0f;
+            }
+            if (stats)
+                stats[e] += 1;
+        }
+    }
+    if (zero_padding) {
+        for (int e = 0; e < E; ++e) {
+            for (int s = expert_offset[e] + num_rows_per_expert[e];
+                 s < expert_offset[e + 1]; ++s) {
+                if (s >= cap) {
+                    err |= EP_ORA_CAPACITY;
+                    continue;
+                }
+                memset((uint8_t *)recv_x + (size_t)s * width, 0, width);
+                if (fp8 == 1)
+                    memset(recv_x_scales + (size_t)s * G, 0, sizeof(float) * (size_t)G);
+                if (recv_src_idx)
+                    recv_src_idx[s] = -1;
+                for (int j = 0; j < K; ++j) {
+                    if (recv_topk_idx)
+                        recv_topk_idx[(size_t)s * K + j] = -1;
+                    if (recv_topk_weights)
+                        recv_topk_weights[(size_t)s * K + j] = 0.0f;
+                }
+            }
+        }
+    }
+    free(q);
+    free(sc);
+    return err;
+}
+
+/*
+ * Expanded combine: out[t] = bf16(bias0 + bias1 + sum over t's rows in
+ * ascending row order of c * y[row]), c = the row's gate weight (or 1).
+ */
+int ora_combine_expanded(const uint16_t *y, int cap, int H, const int32_t *token_slot,
+                         int T, int K, const int64_t *topk_idx,
+                         const float *topk_weights, int E, const uint16_t *bias0,
+                         const uint16_t *bias1, uint16_t *out)
+{
+    int err = 0;
+    float *acc = (float *)malloc(sizeof(float) * (size_t)(H > 0 ? H : 1));
+    for (int t = 0; t < T; ++t) {
+        if (topk_weights && !choices_agree(topk_idx, t, K, E, token_slot))
+            err |= EP_ORA_STALE;
+        for (int h = 0; h < H; ++h) {
+            acc[h] = bias0 ? ora_bf16_to_f32(bias0[(size_t)t * H + h]) : 0.0f;
+            if (bias1)
+                acc[h] = acc[h] + ora_bf16_to_f32(bias1[(size_t)t * H + h]);
+        }
+        /* rows in ascending order: repeatedly take the smallest unused slot */
+        int32_t last = -1;
+        for (;;) {
+            int best = -1;
+            for (int k = 0; k < K; ++k) {
+                int32_t s = token_slot[(size_t)t * K + k];
+                if (s > last && (best < 0 || s < token_slot[(size_t)t * K + best]))
+                    best = k;
+            }
+            if (best < 0)
+                break;
+            int32_t slot = token_slot[(size_t)t * K + best];
+            last = slot;
+            if (slot >= cap) {
+                err |= EP_ORA_CAPACITY;
+                continue;
+            }
+            const uint16_t *row = y + (size_t)slot * H;
+            float c = topk_weights ? topk_weights[(size_t)t * K + best] : 1.0f;
+            for (int h = 0; h < H; ++h) {
+                if (topk_weights) {
+                    float p = c * ora_bf16_to_f32(row[h]);
+                    acc[h] = acc[h] + p;
+                } else {
+                    acc[h] = acc[h] + ora_bf16_to_f32(row[h]);
+                }
+            }
+        }
+        for (int h = 0; h < H; ++h)
+            out[(size_t)t * H + h] = ora_f32_to_bf16(acc[h]);
+    }
+    free(acc);
+    return err;
 }

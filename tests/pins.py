@@ -614,5 +614,154 @@ def check_combine_bias(o):
     assert np.array_equal(out0, plain)
 
 
+# --------------------------------------------------------- expanded layout
+
+def check_expanded_golden(o):
+    g = _golden("expanded_layout_hand.json")
+    base = _golden("layout_dispatch_combine_hand.json")
+    idx = np.array(base["topk_idx"], np.int64)
+    w = np.array(base["topk_weights"], np.float32)
+    _, x = _hand_inputs()
+    E, R = g["num_experts"], g["num_ranks"]
+    for c in g["cases"]:
+        lay = o.get_layout_expanded(idx, E, c["expert_alignment"])
+        assert lay["error"] == 0
+        for k in ("num_rows_per_expert", "expert_offset", "token_slot"):
+            assert np.array_equal(lay[k], np.array(c[k])), k
+        cap = int(lay["expert_offset"][E])
+        d = o.dispatch_expanded(x, idx, w, E, R, lay, False, cap, zero_padding=True)
+        assert d["error"] == 0
+        if "recv_src_idx" in c:
+            assert d["recv_src_idx"].tolist() == c["recv_src_idx"]
+            assert d["recv_topk_idx"].tolist() == c["recv_topk_idx"]
+        for s_ in c.get("padding_rows", []):
+            assert d["recv_src_idx"][s_] == -1 and np.all(d["recv_topk_idx"][s_] == -1)
+            assert not d["recv_x"][s_].any()
+        out, _ = o.combine_expanded(d["recv_x"], lay["token_slot"])
+        assert np.array_equal(out, bf16_bits(g["combine_plain_round_trip"]).reshape(out.shape))
+        out, _ = o.combine_expanded(d["recv_x"], lay["token_slot"], idx, w, E)
+        assert np.array_equal(out, bf16_bits(g["combine_weighted_round_trip"]).reshape(out.shape))
+
+
+def brute_expanded(idx, E, align):
+    """Sort formulation: rows are the first choices sorted by (expert,
+    token, k); each expert's block starts at the aligned prefix."""
+    T, K = idx.shape
+    firsts = []
+    for t in range(T):
+        seen = set()
+        for k in range(K):
+            e = int(idx[t, k])
+            if 0 <= e < E and e not in seen:
+                seen.add(e)
+                firsts.append((e, t, k))
+    firsts.sort()
+    counts = Counter(e for e, _, _ in firsts)
+    offset = [0]
+    for e in range(E):
+        offset.append(offset[-1] + -(-counts.get(e, 0) // align) * align)
+    slot = np.full((T, K), -1, np.int64)
+    seen_in_e = Counter()
+    for e, t, k in firsts:
+        slot[t, k] = offset[e] + seen_in_e[e]
+        seen_in_e[e] += 1
+    return [counts.get(e, 0) for e in range(E)], offset, slot
+
+
+def check_expanded_bruteforce(o):
+    rng = np.random.default_rng(61)
+    for trial in range(200):
+        E = int(rng.integers(1, 13))
+        K = int(rng.integers(1, 6))
+        T = int(rng.integers(0, 12))
+        align = int(rng.choice([1, 2, 3, 4, 8]))
+        idx = rng.integers(-1, E, size=(T, K)).astype(np.int64)     # duplicates and -1
+        if trial % 4 == 0 and T:
+            idx[0, 0] = E + 2                                          # a bad id
+        lay = o.get_layout_expanded(idx, E, align)
+        counts, offset, slot = brute_expanded(idx, E, align)
+        assert list(lay["num_rows_per_expert"]) == counts
+        assert list(lay["expert_offset"]) == offset
+        assert np.array_equal(lay["token_slot"], slot)
+        dup = any(len([e for e in row if 0 <= e < E]) != len({e for e in row if 0 <= e < E}) for row in idx.tolist())
+        bad = bool(((idx < -1) | (idx >= E)).any())
+        assert bool(lay["error"] & 16) == dup and bool(lay["error"] & 1) == bad
+
+
+def check_expanded_dispatch_identities(o):
+    rng = np.random.default_rng(62)
+    T, H, K, E, R = 120, 256, 4, 16, 4
+    epr = E // R
+    idx = _random_idx(rng, T, K, E, p_mask=0.2)
+    w = rng.random((T, K)).astype(np.float32)
+    x = bf16_bits(rng.standard_normal((T, H)).astype(np.float32)).reshape(T, H)
+    for align in (1, 8):
+        lay = o.get_layout_expanded(idx, E, align)
+        cap = int(lay["expert_offset"][E])
+        stats = np.zeros(E, np.uint32)
+        for mode in (False, True, "packed"):
+            d = o.dispatch_expanded(x, idx, w, E, R, lay, mode, cap, zero_padding=True,
+                                    stats=stats if mode is False else None)
+            assert d["error"] == 0
+            occupied = np.zeros(cap, bool)
+            for t in range(T):
+                for k in range(K):
+                    s_ = lay["token_slot"][t, k]
+                    if s_ < 0:
+                        continue
+                    occupied[s_] = True
+                    e = int(idx[t, k])
+                    assert d["recv_src_idx"][s_] == t
+                    exp = np.full(K, -1)
+                    exp[k] = e % epr
+                    assert np.array_equal(d["recv_topk_idx"][s_], exp)
+                    assert d["recv_topk_weights"][s_][k] == w[t, k] and d["recv_topk_weights"][s_].sum() == w[t, k]
+                    if mode is False:
+                        assert np.array_equal(d["recv_x"][s_], x[t])
+                    else:
+                        q, sc = o.quantize_row(x[t])
+                        assert np.array_equal(d["recv_x"][s_][:H], q)
+                        got_sc = d["recv_x_scales"][s_] if mode is True else d["recv_x"][s_][H:H + 4 * (H // 128)].view(np.float32)
+                        assert np.array_equal(got_sc, sc)
+                    # segment of the row's expert
+                    assert lay["expert_offset"][e] <= s_ < lay["expert_offset"][e] + lay["num_rows_per_expert"][e]
+            assert np.all(d["recv_src_idx"][~occupied] == -1) and not d["recv_x"][~occupied].any()
+            assert np.all(d["recv_topk_idx"][~occupied] == -1)
+        assert np.array_equal(stats, np.bincount(idx[idx >= 0], minlength=E))
+        # segments start on aligned rows
+        assert np.all(lay["expert_offset"] % align == 0)
+
+
+def check_expanded_combine(o):
+    # ascending row order: a token's rows in slot order carry 2^24, 1, -2^24
+    y = bf16_bits([[2.0 ** 24], [1.0], [-(2.0 ** 24)]]).reshape(3, 1)
+    slot = np.array([[2, 0, 1]], np.int32)            # k order differs from row order
+    out, _ = o.combine_expanded(np.repeat(y, 8, axis=1), slot)
+    assert np.all(out == 0)
+    out, _ = o.combine_expanded(np.repeat(y[::-1], 8, axis=1), slot)
+    assert np.all(bits_to_f32(out) == 1.0)
+    # closed form round trip: n_t copies of x[t]; within rounding for weights
+    rng = np.random.default_rng(63)
+    T, H, K, E, R = 200, 128, 6, 32, 8
+    idx = _random_idx(rng, T, K, E, p_mask=0.3)
+    idx[:3] = -1
+    w = rng.random((T, K)).astype(np.float32)
+    x = bf16_bits(rng.standard_normal((T, H)).astype(np.float32)).reshape(T, H)
+    lay = o.get_layout_expanded(idx, E, 4)
+    cap = int(lay["expert_offset"][E])
+    d = o.dispatch_expanded(x, idx, w, E, R, lay, False, cap)
+    out, err = o.combine_expanded(d["recv_x"], lay["token_slot"])
+    assert err == 0
+    n = (lay["token_slot"] >= 0).sum(axis=1).astype(np.float32)
+    prod = bits_to_f32(x).reshape(T, H) * n[:, None] + np.float32(0.0)
+    assert np.array_equal(out, torch.from_numpy(prod).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+    outw, _ = o.combine_expanded(d["recv_x"], lay["token_slot"], idx, w, E)
+    wsum = np.where(lay["token_slot"] >= 0, w, 0).sum(axis=1).astype(np.float64)
+    exact = bits_to_f32(x).reshape(T, H).astype(np.float64) * wsum[:, None]
+    got = bits_to_f32(outw).reshape(T, H).astype(np.float64)
+    assert np.all(np.abs(got - exact) <= 2.0 ** -8 * np.abs(exact) + 1e-30)
+    assert np.all(outw[:3] == 0)
+
+
 
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

@@ -83,6 +83,16 @@ MUTANTS = [
      "acc[h] = acc[h] + ora_bf16_to_f32(bias1[(size_t)t * H + h]);", "acc[h] = acc[h];"),
     ("bias_added_after", "int ora_combine_ex",
      "acc[h] = bias0 ? ora_bf16_to_f32(bias0[(size_t)t * H + h]) : 0.0f;", "acc[h] = 0.0f;"),
+    ("expanded_unaligned", "int ora_get_layout_expanded",
+     "int aligned = (rows + align - 1) / align * align;", "int aligned = rows;"),
+    ("expanded_duplicates_kept", "static int first_choice",
+     "if (topk_idx[(size_t)t * K + j] == e)\n            return 0;", "if (topk_idx[(size_t)t * K + j] == e + 999)\n            return 0;"),
+    ("expanded_row_marks_all", "int ora_dispatch_expanded",
+     "int here = j == k && valid_expert(e, E);", "int here = valid_expert(e, E);"),
+    ("expanded_padding_kept", "int ora_dispatch_expanded",
+     "                if (recv_src_idx)\n                    recv_src_idx[s] = -1;", "                if (recv_src_idx)\n                    recv_src_idx[s] = -3;"),
+    ("expanded_combine_k_order", "int ora_combine_expanded",
+     "if (s > last && (best < 0 || s < token_slot[(size_t)t * K + best]))", "if (s > last && best < 0)"),
     ("combine_skips_rank0", "int ora_combine",
      "if (slot < 0)\n                continue;", "if (slot <= 0)\n                continue;"),
 ]
