@@ -22,11 +22,14 @@ import torch
 
 from . import _native as N
 from ._native import (EP_ERRBIT_BAD_INDEX, EP_ERRBIT_CAPACITY,  # noqa: F401
-                      EP_ERRBIT_STALE_LAYOUT, EP_ERRBIT_TIMEOUT, EP_FP8_GROUP)
+                      EP_ERRBIT_DUP_EXPERT, EP_ERRBIT_STALE_LAYOUT, EP_ERRBIT_TIMEOUT,
+                      EP_FP8_GROUP)
 
 __all__ = ["EPError", "Layout", "Dispatched", "ep_layout_workspace_bytes",
            "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch", "ep_dispatch_ex",
-           "ep_combine", "ep_combine_ex", "ep_fp8_packed_row_bytes", "library_path"]
+           "ep_combine", "ep_combine_ex", "ep_fp8_packed_row_bytes", "ExpandedLayout",
+           "ep_expanded_layout_workspace_bytes", "ep_get_layout_expanded",
+           "ep_dispatch_expanded", "ep_combine_expanded", "library_path"]
 
 
 class EPError(RuntimeError):
@@ -293,3 +296,146 @@ def ep_combine(y: torch.Tensor, layout: Layout, topk_idx: Optional[torch.Tensor]
 
 
 ep_combine_ex = ep_combine
+
+
+# ------------------------------------------------------------------ expanded
+
+def ep_expanded_layout_workspace_bytes(num_tokens: int, num_experts: int) -> int:
+    return int(N.load().ep_expanded_layout_workspace_bytes(num_tokens, num_experts))
+
+
+@dataclass
+class ExpandedLayout:
+    """Device tensors of an expanded (one row per (token, expert)) layout."""
+    num_rows_per_expert: torch.Tensor  # int32 [E]
+    expert_offset: torch.Tensor        # int32 [E+1]
+    token_slot: torch.Tensor           # int32 [T, K]
+    error_word: torch.Tensor           # int32 [1]
+    workspace: torch.Tensor            # uint8, zero-filled once
+    num_tokens: int
+    num_topk: int
+    num_experts: int
+    expert_alignment: int
+
+    @staticmethod
+    def empty(num_tokens: int, num_topk: int, num_experts: int, expert_alignment: int,
+              device) -> "ExpandedLayout":
+        dev = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        ws = ep_expanded_layout_workspace_bytes(num_tokens, num_experts)
+        return ExpandedLayout(
+            torch.empty(num_experts, **i32), torch.empty(num_experts + 1, **i32),
+            torch.empty((num_tokens, num_topk), **i32), torch.zeros(1, **i32),
+            torch.zeros(max(ws, 16), dtype=torch.uint8, device=dev),
+            num_tokens, num_topk, num_experts, expert_alignment)
+
+    def c_struct(self) -> N.ep_expanded_layout_t:
+        return N.ep_expanded_layout_t(
+            self.num_rows_per_expert.data_ptr(), self.expert_offset.data_ptr(),
+            self.token_slot.data_ptr(), self.error_word.data_ptr())
+
+    def num_rows(self) -> int:
+        """Rows including padding, read back to the host (synchronises)."""
+        return int(self.expert_offset[self.num_experts].item())
+
+    def errors(self) -> int:
+        return int(self.error_word.item()) & 0xffffffff
+
+    def capacity_bound(self) -> int:
+        """Rows that always suffice, without a read-back."""
+        return self.num_tokens * self.num_topk + self.num_experts * (self.expert_alignment - 1)
+
+
+def ep_get_layout_expanded(topk_idx: torch.Tensor, num_experts: int, expert_alignment: int = 1,
+                           layout: Optional[ExpandedLayout] = None, stream=None) -> ExpandedLayout:
+    _want(topk_idx, "topk_idx", torch.int64)
+    T, K = topk_idx.shape
+    dev = topk_idx.device
+    if layout is None:
+        layout = ExpandedLayout.empty(T, K, num_experts, expert_alignment, dev)
+    elif (layout.num_tokens, layout.num_topk, layout.num_experts) != (T, K, num_experts):
+        raise ValueError("layout was allocated for other sizes")
+    layout.expert_alignment = expert_alignment
+    st = layout.c_struct()
+    _check(N.load().ep_get_layout_expanded(
+        _ptr(topk_idx), T, K, num_experts, expert_alignment, C.byref(st), _ptr(layout.workspace),
+        layout.workspace.numel(), _stream(stream, dev)), "ep_get_layout_expanded")
+    return layout
+
+
+def ep_dispatch_expanded(x: torch.Tensor, topk_idx: torch.Tensor,
+                         topk_weights: Optional[torch.Tensor], layout: ExpandedLayout,
+                         num_ranks: int, dtype: str = "bf16", recv_capacity: Optional[int] = None,
+                         zero_padding: bool = True, out: Optional[Dispatched] = None,
+                         metadata: bool = True,
+                         cumulative_recv_stats: Optional[torch.Tensor] = None,
+                         stream=None) -> Dispatched:
+    """One row per (token, expert), grouped by expert (see ExpandedLayout)."""
+    _want(x, "x", torch.bfloat16)
+    dev = x.device
+    _want(topk_idx, "topk_idx", torch.int64, dev)
+    T, H = x.shape
+    K = topk_idx.shape[1]
+    E = layout.num_experts
+    code = _DTYPES[dtype]
+    fp8 = code != N.EP_DTYPE_BF16
+    packed = code == N.EP_DTYPE_FP8_E4M3_PACKED
+    if recv_capacity is None:
+        recv_capacity = out.recv_x.shape[0] if out is not None else layout.capacity_bound()
+    if out is None:
+        if packed:
+            rx = torch.empty((recv_capacity, ep_fp8_packed_row_bytes(H)), dtype=torch.uint8, device=dev)
+        else:
+            rx = torch.empty((recv_capacity, H), dtype=torch.float8_e4m3fn if fp8 else torch.bfloat16,
+                             device=dev)
+        out = Dispatched(
+            rx,
+            torch.empty((recv_capacity, H // EP_FP8_GROUP), dtype=torch.float32, device=dev)
+            if fp8 and not packed else None,
+            torch.empty(recv_capacity, dtype=torch.int32, device=dev) if metadata else None,
+            torch.empty((recv_capacity, K), dtype=torch.int32, device=dev) if metadata else None,
+            torch.empty((recv_capacity, K), dtype=torch.float32, device=dev)
+            if metadata and topk_weights is not None else None)
+    if topk_weights is not None:
+        _want(topk_weights, "topk_weights", torch.float32, dev)
+    st = layout.c_struct()
+    args = N.ep_dispatch_expanded_args_t(
+        x.data_ptr(), T, H, topk_idx.data_ptr(),
+        None if topk_weights is None else topk_weights.data_ptr(), K, E, num_ranks,
+        C.pointer(st), code, out.recv_x.data_ptr(),
+        None if out.recv_x_scales is None else out.recv_x_scales.data_ptr(),
+        None if out.recv_src_idx is None else out.recv_src_idx.data_ptr(),
+        None if out.recv_topk_idx is None else out.recv_topk_idx.data_ptr(),
+        None if out.recv_topk_weights is None else out.recv_topk_weights.data_ptr(),
+        recv_capacity, 1 if zero_padding else 0,
+        None if cumulative_recv_stats is None else cumulative_recv_stats.data_ptr())
+    _check(N.load().ep_dispatch_expanded(C.byref(args), _stream(stream, dev)), "ep_dispatch_expanded")
+    return out
+
+
+def ep_combine_expanded(y: torch.Tensor, layout: ExpandedLayout,
+                        topk_idx: Optional[torch.Tensor] = None,
+                        topk_weights: Optional[torch.Tensor] = None,
+                        out: Optional[torch.Tensor] = None, bias0: Optional[torch.Tensor] = None,
+                        bias1: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out[t] = bf16(bias0 + bias1 + sum over t's rows, ascending, of c * y[row])."""
+    _want(y, "y", torch.bfloat16)
+    dev = y.device
+    cap, H = y.shape
+    T, K = layout.num_tokens, layout.num_topk
+    if (topk_idx is None) != (topk_weights is None):
+        raise ValueError("pass both topk_idx and topk_weights, or neither")
+    if topk_idx is not None:
+        _want(topk_idx, "topk_idx", torch.int64, dev)
+        _want(topk_weights, "topk_weights", torch.float32, dev)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    st = layout.c_struct()
+    args = N.ep_combine_expanded_args_t(
+        y.data_ptr(), cap, H, C.pointer(st), T, K,
+        None if topk_idx is None else topk_idx.data_ptr(),
+        None if topk_weights is None else topk_weights.data_ptr(), layout.num_experts,
+        None if bias0 is None else bias0.data_ptr(), None if bias1 is None else bias1.data_ptr(),
+        out.data_ptr())
+    _check(N.load().ep_combine_expanded(C.byref(args), _stream(stream, dev)), "ep_combine_expanded")
+    return out

@@ -25,6 +25,7 @@ EP_ERRBIT_BAD_INDEX = 0x1
 EP_ERRBIT_CAPACITY = 0x2
 EP_ERRBIT_TIMEOUT = 0x4
 EP_ERRBIT_STALE_LAYOUT = 0x8
+EP_ERRBIT_DUP_EXPERT = 0x10
 
 EP_MAX_RANKS = 64
 EP_MAX_TOPK = 32
@@ -67,6 +68,38 @@ class ep_combine_args_t(C.Structure):
     ]
 
 
+class ep_expanded_layout_t(C.Structure):
+    _fields_ = [
+        ("num_rows_per_expert", C.c_void_p),
+        ("expert_offset", C.c_void_p),
+        ("token_slot", C.c_void_p),
+        ("error_word", C.c_void_p),
+    ]
+
+
+class ep_dispatch_expanded_args_t(C.Structure):
+    _fields_ = [
+        ("x", C.c_void_p), ("num_tokens", C.c_int), ("hidden", C.c_int),
+        ("topk_idx", C.c_void_p), ("topk_weights", C.c_void_p), ("num_topk", C.c_int),
+        ("num_experts", C.c_int), ("num_ranks", C.c_int),
+        ("layout", C.POINTER(ep_expanded_layout_t)), ("dtype", C.c_int),
+        ("recv_x", C.c_void_p), ("recv_x_scales", C.c_void_p), ("recv_src_idx", C.c_void_p),
+        ("recv_topk_idx", C.c_void_p), ("recv_topk_weights", C.c_void_p),
+        ("recv_capacity", C.c_int), ("zero_padding", C.c_int),
+        ("cumulative_recv_stats", C.c_void_p),
+    ]
+
+
+class ep_combine_expanded_args_t(C.Structure):
+    _fields_ = [
+        ("y", C.c_void_p), ("recv_capacity", C.c_int), ("hidden", C.c_int),
+        ("layout", C.POINTER(ep_expanded_layout_t)), ("num_tokens", C.c_int),
+        ("num_topk", C.c_int), ("topk_idx", C.c_void_p), ("topk_weights", C.c_void_p),
+        ("num_experts", C.c_int), ("bias0", C.c_void_p), ("bias1", C.c_void_p),
+        ("out", C.c_void_p),
+    ]
+
+
 # name -> (restype, argtypes); mirrors include/ep_gb300.h
 _p, _i, _sz = C.c_void_p, C.c_int, C.c_size_t
 _LP = C.POINTER(ep_layout_t)
@@ -79,6 +112,10 @@ SIGNATURES = {
     "ep_fp8_packed_row_bytes": (_sz, [_i]),
     "ep_dispatch_ex": (_i, [C.POINTER(ep_dispatch_args_t), _p]),
     "ep_combine_ex": (_i, [C.POINTER(ep_combine_args_t), _p]),
+    "ep_expanded_layout_workspace_bytes": (_sz, [_i, _i]),
+    "ep_get_layout_expanded": (_i, [_p, _i, _i, _i, _i, C.POINTER(ep_expanded_layout_t), _p, _sz, _p]),
+    "ep_dispatch_expanded": (_i, [C.POINTER(ep_dispatch_expanded_args_t), _p]),
+    "ep_combine_expanded": (_i, [C.POINTER(ep_combine_expanded_args_t), _p]),
     "ep_status_str": (C.c_char_p, [_i]),
     "ep_last_error": (C.c_char_p, []),
     "ep_abi_version": (_i, []),

@@ -22,7 +22,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libep_gb300.so")
 
-SOURCES = ["ep_api.cu", "ep_layout.cu", "ep_dispatch.cu", "ep_combine.cu", "ep_noalloc.cu"]
+SOURCES = ["ep_api.cu", "ep_layout.cu", "ep_layout_expanded.cu", "ep_dispatch.cu", "ep_combine.cu",
+           "ep_noalloc.cu"]
 HEADERS = ["ep_device.cuh", "ep_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",

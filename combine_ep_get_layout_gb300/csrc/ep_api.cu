@@ -194,6 +194,10 @@ ep_status_t ep_dispatch_ex(const ep_dispatch_args_t *args, ep_stream_t stream) {
   a.topk_weights = x.topk_weights;
   a.token_slot = x.layout->token_slot;
   a.error_word = x.layout->error_word;
+  a.expanded = false;
+  a.expert_offset = nullptr;
+  a.num_rows_per_expert = nullptr;
+  a.zero_padding = false;
   a.fp8 = fp8;
   a.packed_row_bytes = packed ? (int)fp8_packed_row_bytes(x.hidden) : 0;
   a.recv_x = x.recv_x;
@@ -254,6 +258,7 @@ ep_status_t ep_combine_ex(const ep_combine_args_t *args, ep_stream_t stream) {
   a.hidden = x.hidden;
   a.num_tokens = x.num_tokens;
   a.num_ranks = x.num_ranks;
+  a.expanded = false;
   a.num_topk = weighted ? x.num_topk : 0;
   a.num_experts = weighted ? x.num_experts : x.num_ranks;
   a.token_slot = x.layout->token_slot;
@@ -272,6 +277,151 @@ ep_status_t ep_combine(const void *y, int recv_capacity, int hidden, const ep_la
   const ep_combine_args_t a = {y,        recv_capacity, hidden,       layout,  num_tokens, num_ranks, topk_idx,
                                topk_weights, num_topk,  num_experts,  nullptr, nullptr,    out};
   return ep_combine_ex(&a, stream);
+}
+
+size_t ep_expanded_layout_workspace_bytes(int num_tokens, int num_experts) {
+  if (num_tokens < 0 || num_experts < 1 || num_experts > EP_MAX_EXPERTS) return 0;
+  return expanded_layout_workspace_bytes(num_tokens, num_experts);
+}
+
+ep_status_t ep_get_layout_expanded(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
+                                   int expert_alignment, const ep_expanded_layout_t *layout, void *workspace,
+                                   size_t workspace_bytes, ep_stream_t stream) {
+  static const char *fn = "ep_get_layout_expanded";
+  clear_error();
+  if (num_tokens < 0) return fail(EP_ERR_INVALID_ARG, "%s: num_tokens=%d < 0", fn, num_tokens);
+  if (num_topk < 1 || num_topk > EP_MAX_TOPK)
+    return fail(num_topk < 1 ? EP_ERR_INVALID_ARG : EP_ERR_UNSUPPORTED, "%s: num_topk=%d not in [1, %d]", fn,
+                num_topk, EP_MAX_TOPK);
+  if (num_experts < 1 || num_experts > EP_MAX_EXPERTS)
+    return fail(num_experts < 1 ? EP_ERR_INVALID_ARG : EP_ERR_UNSUPPORTED, "%s: num_experts=%d not in [1, %d]",
+                fn, num_experts, EP_MAX_EXPERTS);
+  if (expert_alignment < 1 || expert_alignment > 4096)
+    return fail(EP_ERR_INVALID_ARG, "%s: expert_alignment=%d not in [1, 4096]", fn, expert_alignment);
+  const bool any = num_tokens > 0;
+  EP_CHECK(check_ptr(fn, "topk_idx", topk_idx, 8, any));
+  if (layout == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: layout is NULL", fn);
+  EP_CHECK(check_ptr(fn, "layout.num_rows_per_expert", layout->num_rows_per_expert, 4, true));
+  EP_CHECK(check_ptr(fn, "layout.expert_offset", layout->expert_offset, 4, true));
+  EP_CHECK(check_ptr(fn, "layout.token_slot", layout->token_slot, 16, any));
+  EP_CHECK(check_ptr(fn, "layout.error_word", layout->error_word, 4, true));
+  EP_CHECK(check_ptr(fn, "workspace", workspace, 16, true));
+  const size_t need = expanded_layout_workspace_bytes(num_tokens, num_experts);
+  if (workspace_bytes < need)
+    return fail(EP_ERR_INVALID_ARG, "%s: workspace_bytes=%zu < %zu needed", fn, workspace_bytes, need);
+  return launch_layout_expanded(topk_idx, num_tokens, num_topk, num_experts, expert_alignment, *layout,
+                                workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ep_status_t ep_dispatch_expanded(const ep_dispatch_expanded_args_t *args, ep_stream_t stream) {
+  static const char *fn = "ep_dispatch_expanded";
+  clear_error();
+  if (args == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: args is NULL", fn);
+  const ep_dispatch_expanded_args_t &x = *args;
+  if (x.num_tokens < 0) return fail(EP_ERR_INVALID_ARG, "%s: num_tokens=%d < 0", fn, x.num_tokens);
+  if (x.dtype != EP_DTYPE_BF16 && x.dtype != EP_DTYPE_FP8_E4M3 && x.dtype != EP_DTYPE_FP8_E4M3_PACKED)
+    return fail(EP_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)x.dtype);
+  const bool fp8 = x.dtype != EP_DTYPE_BF16;
+  const bool packed = x.dtype == EP_DTYPE_FP8_E4M3_PACKED;
+  if (x.hidden < 1) return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d < 1", fn, x.hidden);
+  if (x.hidden > EP_MAX_HIDDEN)
+    return fail(EP_ERR_UNSUPPORTED, "%s: hidden=%d > %d", fn, x.hidden, EP_MAX_HIDDEN);
+  if (x.hidden % (fp8 ? EP_FP8_GROUP : 8) != 0)
+    return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d is not a multiple of %d", fn, x.hidden,
+                fp8 ? EP_FP8_GROUP : 8);
+  EP_CHECK(check_routing_sizes(fn, x.num_topk, x.num_experts, x.num_ranks));
+  if (x.recv_capacity < 0) return fail(EP_ERR_INVALID_ARG, "%s: recv_capacity=%d < 0", fn, x.recv_capacity);
+  const bool any = x.num_tokens > 0;
+  const bool rows = x.recv_capacity > 0;
+  EP_CHECK(check_ptr(fn, "x", x.x, 16, any));
+  EP_CHECK(check_ptr(fn, "topk_idx", x.topk_idx, 8, any));
+  if (x.layout == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: layout is NULL", fn);
+  EP_CHECK(check_ptr(fn, "layout.token_slot", x.layout->token_slot, 4, any));
+  EP_CHECK(check_ptr(fn, "layout.error_word", x.layout->error_word, 4, true));
+  EP_CHECK(check_ptr(fn, "layout.expert_offset", x.layout->expert_offset, 4, x.zero_padding != 0));
+  EP_CHECK(check_ptr(fn, "layout.num_rows_per_expert", x.layout->num_rows_per_expert, 4, x.zero_padding != 0));
+  EP_CHECK(check_ptr(fn, "recv_x", x.recv_x, 16, rows));
+  EP_CHECK(check_ptr(fn, "recv_x_scales", x.recv_x_scales, 4, fp8 && !packed && rows));
+  EP_CHECK(check_ptr(fn, "recv_src_idx", x.recv_src_idx, 4, false));
+  EP_CHECK(check_ptr(fn, "recv_topk_idx", x.recv_topk_idx, 4, false));
+  EP_CHECK(check_ptr(fn, "recv_topk_weights", x.recv_topk_weights, 4, false));
+  EP_CHECK(check_ptr(fn, "topk_weights", x.topk_weights, 4, any && x.recv_topk_weights != nullptr));
+  EP_CHECK(check_ptr(fn, "cumulative_recv_stats", x.cumulative_recv_stats, 4, false));
+  DispatchArgs a;
+  a.x = static_cast<const uint16_t *>(x.x);
+  a.num_tokens = x.num_tokens;
+  a.hidden = x.hidden;
+  a.num_topk = x.num_topk;
+  a.num_experts = x.num_experts;
+  a.num_ranks = x.num_ranks;
+  a.topk_idx = x.topk_idx;
+  a.topk_weights = x.topk_weights;
+  a.token_slot = x.layout->token_slot;
+  a.error_word = x.layout->error_word;
+  a.expanded = true;
+  a.expert_offset = x.layout->expert_offset;
+  a.num_rows_per_expert = x.layout->num_rows_per_expert;
+  a.zero_padding = x.zero_padding != 0;
+  a.fp8 = fp8;
+  a.packed_row_bytes = packed ? (int)fp8_packed_row_bytes(x.hidden) : 0;
+  a.recv_x = x.recv_x;
+  a.recv_x_scales = packed ? nullptr : x.recv_x_scales;
+  a.recv_src_idx = x.recv_src_idx;
+  a.recv_topk_idx = x.recv_topk_idx;
+  a.recv_topk_weights = x.recv_topk_weights;
+  a.recv_capacity = x.recv_capacity;
+  a.recv_stats = x.cumulative_recv_stats;
+  return launch_dispatch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ep_status_t ep_combine_expanded(const ep_combine_expanded_args_t *args, ep_stream_t stream) {
+  static const char *fn = "ep_combine_expanded";
+  clear_error();
+  if (args == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: args is NULL", fn);
+  const ep_combine_expanded_args_t &x = *args;
+  if (x.num_tokens < 0) return fail(EP_ERR_INVALID_ARG, "%s: num_tokens=%d < 0", fn, x.num_tokens);
+  if (x.recv_capacity < 0) return fail(EP_ERR_INVALID_ARG, "%s: recv_capacity=%d < 0", fn, x.recv_capacity);
+  if (x.hidden < 1) return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d < 1", fn, x.hidden);
+  if (x.hidden > EP_MAX_HIDDEN)
+    return fail(EP_ERR_UNSUPPORTED, "%s: hidden=%d > %d", fn, x.hidden, EP_MAX_HIDDEN);
+  if (x.hidden % 8 != 0) return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d is not a multiple of 8", fn, x.hidden);
+  if (x.num_topk < 1 || x.num_topk > EP_MAX_TOPK)
+    return fail(x.num_topk < 1 ? EP_ERR_INVALID_ARG : EP_ERR_UNSUPPORTED, "%s: num_topk=%d not in [1, %d]", fn,
+                x.num_topk, EP_MAX_TOPK);
+  const bool weighted = x.topk_weights != nullptr;
+  if ((x.topk_idx == nullptr) != (x.topk_weights == nullptr))
+    return fail(EP_ERR_INVALID_ARG, "%s: topk_idx and topk_weights must both be given or both be NULL", fn);
+  const bool any = x.num_tokens > 0;
+  if (weighted) {
+    if (x.num_experts < 1 || x.num_experts > EP_MAX_EXPERTS)
+      return fail(EP_ERR_INVALID_ARG, "%s: num_experts=%d not in [1, %d]", fn, x.num_experts, EP_MAX_EXPERTS);
+    EP_CHECK(check_ptr(fn, "topk_idx", x.topk_idx, 8, any));
+    EP_CHECK(check_ptr(fn, "topk_weights", x.topk_weights, 4, any));
+  }
+  EP_CHECK(check_ptr(fn, "y", x.y, 16, x.recv_capacity > 0 && any));
+  if (x.layout == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: layout is NULL", fn);
+  EP_CHECK(check_ptr(fn, "layout.token_slot", x.layout->token_slot, 4, any));
+  EP_CHECK(check_ptr(fn, "layout.error_word", x.layout->error_word, 4, true));
+  EP_CHECK(check_ptr(fn, "out", x.out, 16, any));
+  EP_CHECK(check_ptr(fn, "bias0", x.bias0, 16, false));
+  EP_CHECK(check_ptr(fn, "bias1", x.bias1, 16, false));
+  CombineArgs a;
+  a.y = static_cast<const uint16_t *>(x.y);
+  a.recv_capacity = x.recv_capacity;
+  a.hidden = x.hidden;
+  a.num_tokens = x.num_tokens;
+  a.num_ranks = 1;  // unused by the expanded reduce
+  a.expanded = true;
+  a.num_topk = x.num_topk;
+  a.num_experts = weighted ? x.num_experts : 1;
+  a.token_slot = x.layout->token_slot;
+  a.error_word = x.layout->error_word;
+  a.topk_idx = x.topk_idx;
+  a.topk_weights = x.topk_weights;
+  a.bias0 = static_cast<const uint16_t *>(x.bias0);
+  a.bias1 = static_cast<const uint16_t *>(x.bias1);
+  a.out = static_cast<uint16_t *>(x.out);
+  return launch_combine(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char *ep_status_str(ep_status_t status) {

@@ -29,7 +29,9 @@ constexpr int kCombineCols = 1;  // 16-byte columns per thread per pass
 struct CombineParams {
   const uint16_t *y;
   int cap, H, T, R, K, E, epr;
-  const int32_t *token_slot;
+  int D;          // destinations per token: R ranks, or K rows (expanded)
+  bool expanded;  // token_slot is [T * K]: one row per (token, expert)
+  const int32_t *token_slot;  // [T * D]
   uint32_t *error_word;
   const int64_t *topk_idx;
   const float *topk_weights;
@@ -69,6 +71,41 @@ __device__ __forceinline__ void accumulate(float (&acc)[8], int4 v, float c) {
   }
 }
 
+// Warp-collective: the layout holds exactly this routing's rows (lane j:
+// the slot of destination j; e: the expert of top-k slot lane, -1 past K).
+__device__ __forceinline__ bool layout_agrees(const CombineParams &p, int64_t e, int slot_lo, int slot_hi,
+                                              int lane) {
+  return p.expanded ? choices_agree(e, p.E, p.K, slot_lo, lane)
+                    : ranks_agree(e, p.E, p.epr, p.R, slot_lo, slot_hi, lane);
+}
+
+// Warp-collective: the coefficient of destination `lane`.  A rank row: the
+// fp32 sum, in k order, of the weights of the token's experts on that rank.
+// An expanded row: its own gate weight.
+__device__ __forceinline__ float coefficient(const CombineParams &p, int64_t e_lane, float w_lane, int lane) {
+  if (p.expanded) return w_lane;
+  float coef = 0.0f;
+  for (int k = 0; k < p.K; ++k) {
+    const int64_t e = __shfl_sync(0xffffffffu, e_lane, k);
+    const float w = __shfl_sync(0xffffffffu, w_lane, k);
+    if (e >= 0 && e < p.E && static_cast<int>(e) / p.epr == lane) coef = __fadd_rn(coef, w);
+  }
+  return coef;
+}
+
+// Warp-collective: where destination `lane` goes among the token's rows
+// (bal: the lanes with a row).  Rank rows in ascending rank (lane) order;
+// expanded rows in ascending row order.
+__device__ __forceinline__ int row_position(const CombineParams &p, int slot, uint32_t bal, uint32_t lanes_below) {
+  if (!p.expanded) return __popc(bal & lanes_below);
+  int pos = 0;
+  for (int j = 0; j < p.D; ++j) {
+    const int s = __shfl_sync(0xffffffffu, slot, j);
+    pos += (s >= 0 && s < slot) ? 1 : 0;
+  }
+  return pos;
+}
+
 template <bool WEIGHTED>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams p) {
   __shared__ int32_t s_slot[2][EP_MAX_RANKS];
@@ -87,40 +124,59 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
   for (int t = blockIdx.x; t < p.T; t += gridDim.x, ++i) {
     const int b = i & 1;
     if (warp == 0) {
-      if (WEIGHTED) {
-        const int64_t e = lane < p.K ? __ldg(p.topk_idx + (size_t)t * p.K + lane) : -1;
-        const int lo = lane < p.R ? __ldg(p.token_slot + (size_t)t * p.R + lane) : -1;
-        const int hi = lane + kWarpSize < p.R ? __ldg(p.token_slot + (size_t)t * p.R + lane + kWarpSize) : -1;
-        if (!ranks_agree(e, p.E, p.epr, p.R, lo, hi, lane) && lane == 0)
-          set_error(p.error_word, EP_ERRBIT_STALE_LAYOUT);
-      }
       int count = 0;
-      for (int r0 = 0; r0 < p.R; r0 += kWarpSize) {
-        const int r = r0 + lane;
-        int slot = -1;
-        float c = 1.0f;
-        if (r < p.R) {
-          slot = __ldg(p.token_slot + (size_t)t * p.R + r);
-          if (slot >= p.cap) {
-            set_error(p.error_word, EP_ERRBIT_CAPACITY);
-            slot = -1;
-          }
-          if (WEIGHTED && slot >= 0) {
-            c = 0.0f;
-            for (int k = 0; k < p.K; ++k) {
-              const int64_t e = __ldg(p.topk_idx + (size_t)t * p.K + k);
-              if (e >= 0 && e < p.E && static_cast<int>(e) / p.epr == r)
-                c = __fadd_rn(c, __ldg(p.topk_weights + (size_t)t * p.K + k));
-            }
-          }
+      if (p.expanded) {  // one pass: K <= 32 rows, placed in ascending row order
+        int slot = lane < p.D ? __ldg(p.token_slot + (size_t)t * p.D + lane) : -1;
+        const int64_t e = (WEIGHTED && lane < p.K) ? __ldg(p.topk_idx + (size_t)t * p.K + lane) : -1;
+        const float w = (WEIGHTED && lane < p.K) ? __ldg(p.topk_weights + (size_t)t * p.K + lane) : 0.0f;
+        if (WEIGHTED && !layout_agrees(p, e, slot, -1, lane) && lane == 0)
+          set_error(p.error_word, EP_ERRBIT_STALE_LAYOUT);
+        if (slot >= p.cap) {
+          set_error(p.error_word, EP_ERRBIT_CAPACITY);
+          slot = -1;
         }
         const uint32_t bal = __ballot_sync(0xffffffffu, slot >= 0);
+        const int pos = row_position(p, slot, bal, lanes_below);
         if (slot >= 0) {
-          const int pos = count + __popc(bal & lanes_below);
           s_slot[b][pos] = slot;
-          s_coef[b][pos] = c;
+          s_coef[b][pos] = WEIGHTED ? w : 1.0f;
         }
-        count += __popc(bal);
+        count = __popc(bal);
+      } else {
+        if (WEIGHTED) {
+          const int64_t e = lane < p.K ? __ldg(p.topk_idx + (size_t)t * p.K + lane) : -1;
+          const int lo = lane < p.R ? __ldg(p.token_slot + (size_t)t * p.R + lane) : -1;
+          const int hi = lane + kWarpSize < p.R ? __ldg(p.token_slot + (size_t)t * p.R + lane + kWarpSize) : -1;
+          if (!ranks_agree(e, p.E, p.epr, p.R, lo, hi, lane) && lane == 0)
+            set_error(p.error_word, EP_ERRBIT_STALE_LAYOUT);
+        }
+        for (int r0 = 0; r0 < p.R; r0 += kWarpSize) {
+          const int r = r0 + lane;
+          int slot = -1;
+          float c = 1.0f;
+          if (r < p.R) {
+            slot = __ldg(p.token_slot + (size_t)t * p.R + r);
+            if (slot >= p.cap) {
+              set_error(p.error_word, EP_ERRBIT_CAPACITY);
+              slot = -1;
+            }
+            if (WEIGHTED && slot >= 0) {
+              c = 0.0f;
+              for (int k = 0; k < p.K; ++k) {
+                const int64_t e = __ldg(p.topk_idx + (size_t)t * p.K + k);
+                if (e >= 0 && e < p.E && static_cast<int>(e) / p.epr == r)
+                  c = __fadd_rn(c, __ldg(p.topk_weights + (size_t)t * p.K + k));
+              }
+            }
+          }
+          const uint32_t bal = __ballot_sync(0xffffffffu, slot >= 0);
+          if (slot >= 0) {
+            const int pos = count + __popc(bal & lanes_below);
+            s_slot[b][pos] = slot;
+            s_coef[b][pos] = c;
+          }
+          count += __popc(bal);
+        }
       }
       if (lane == 0) s_n[b] = count;
     }
@@ -205,7 +261,7 @@ struct TokenMeta {
 
 __device__ __forceinline__ TokenMeta fetch_meta(const CombineParams &p, int t, int lane, bool weighted) {
   TokenMeta m;
-  m.slot = lane < p.R ? __ldg(p.token_slot + (size_t)t * p.R + lane) : -1;
+  m.slot = lane < p.D ? __ldg(p.token_slot + (size_t)t * p.D + lane) : -1;
   m.e = (weighted && lane < p.K) ? __ldg(p.topk_idx + (size_t)t * p.K + lane) : -1;
   m.w = (weighted && lane < p.K) ? __ldg(p.topk_weights + (size_t)t * p.K + lane) : 0.0f;
   return m;
@@ -248,26 +304,16 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
       TokenMeta nxt = cur;
       if (j + 1 < ntok) nxt = fetch_meta(p, t + gridDim.x, lane, WEIGHTED);  // in flight meanwhile
       int slot = cur.slot;
-      if (WEIGHTED && !ranks_agree(cur.e, p.E, p.epr, p.R, slot, -1, lane) && lane == 0)
+      if (WEIGHTED && !layout_agrees(p, cur.e, slot, -1, lane) && lane == 0)
         set_error(p.error_word, EP_ERRBIT_STALE_LAYOUT);
       if (slot >= p.cap) {
         set_error(p.error_word, EP_ERRBIT_CAPACITY);
         slot = -1;
       }
-      float coef = 1.0f;
-      if (WEIGHTED) {
-        // rank `lane`'s coefficient: the fp32 sum, in k order, of the weights
-        // of the token's experts on that rank
-        coef = 0.0f;
-        for (int k = 0; k < p.K; ++k) {
-          const int64_t e = __shfl_sync(0xffffffffu, cur.e, k);
-          const float w = __shfl_sync(0xffffffffu, cur.w, k);
-          if (e >= 0 && e < p.E && static_cast<int>(e) / p.epr == lane) coef = __fadd_rn(coef, w);
-        }
-      }
+      const float coef = WEIGHTED ? coefficient(p, cur.e, cur.w, lane) : 1.0f;
       const uint32_t bal = __ballot_sync(0xffffffffu, slot >= 0);
       const int nrows = __popc(bal);
-      const int pos = __popc(bal & lanes_below);
+      const int pos = row_position(p, slot, bal, lanes_below);
       for (int c = 0; c < nchunk; ++c, ++i) {
         const int s = static_cast<int>(i % kCombineStages);
         const int elems = min(kChunk, p.H - c * kChunk);
@@ -410,7 +456,9 @@ ep_status_t launch_combine(const CombineArgs &a, cudaStream_t stream) {
   p.R = a.num_ranks;
   p.K = a.num_topk;
   p.E = a.num_experts;
-  p.epr = (a.topk_weights != nullptr) ? a.num_experts / a.num_ranks : 1;
+  p.epr = (a.topk_weights != nullptr && !a.expanded) ? a.num_experts / a.num_ranks : 1;
+  p.expanded = a.expanded;
+  p.D = a.expanded ? a.num_topk : a.num_ranks;
   p.token_slot = a.token_slot;
   p.error_word = a.error_word;
   p.topk_idx = a.topk_idx;
@@ -419,7 +467,7 @@ ep_status_t launch_combine(const CombineArgs &a, cudaStream_t stream) {
   p.bias1 = a.bias1;
   p.out = a.out;
   const bool weighted = a.topk_weights != nullptr;
-  if (kUseWsCombine && a.num_ranks <= kWsMaxRanks)
+  if (kUseWsCombine && p.D <= kWsMaxRanks)
     return weighted ? launch_ws<true>(p, *di, stream) : launch_ws<false>(p, *di, stream);
   return weighted ? launch_impl<true>(p, *di, stream) : launch_impl<false>(p, *di, stream);
 }

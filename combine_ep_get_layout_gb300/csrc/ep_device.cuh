@@ -176,6 +176,51 @@ __device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
   return d;
 }
 
+// ------------------------------------------------------------- grid barrier
+// For cooperative launches (all blocks co-resident).  The two words live in
+// caller-zeroed global memory; the last block out resets them, so the next
+// launch finds them zero again.
+
+struct GridBarrierWords {
+  uint32_t arrive;
+  uint32_t depart;
+};
+
+// Every thread of every block calls it.  Returns false (in every thread of
+// the block) if the wait gave up after kWaitLimitNs.  `s_flag` is a shared
+// int the block uses to broadcast the outcome.
+__device__ __forceinline__ bool grid_barrier(GridBarrierWords *bar, int *s_flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(&bar->arrive, 1u);
+    int ok = 1;
+    const uint64_t t0 = global_timer_ns();
+    while (ld_acquire_gpu(&bar->arrive) < gridDim.x) {
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        ok = 0;
+        break;
+      }
+      __nanosleep(32);
+    }
+    __threadfence();
+    *s_flag = ok;
+  }
+  __syncthreads();
+  return *s_flag != 0;
+}
+
+// Called once per block, after the block's last use of the barrier.
+__device__ __forceinline__ void grid_barrier_exit(GridBarrierWords *bar) {
+  if (threadIdx.x == 0) {
+    const uint32_t prev = atomicAdd(&bar->depart, 1u);
+    if (prev == gridDim.x - 1u) {
+      atomicExch(&bar->arrive, 0u);
+      atomicExch(&bar->depart, 0u);
+    }
+  }
+}
+
 // ------------------------------------------------- programmatic dependent launch
 // A kernel launched with programmatic stream serialization may start before
 // the kernel ahead of it in the stream has finished; it must wait here before
@@ -201,6 +246,16 @@ __device__ __forceinline__ bool ranks_agree(int64_t e, int E, int epr, int R, in
   bool ok = true;
   if (lane < R) ok = (((mask >> lane) & 1ull) != 0) == (slot_lo >= 0);
   if (lane + 32 < R) ok = ok && ((((mask >> (lane + 32)) & 1ull) != 0) == (slot_hi >= 0));
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Warp-collective, expanded layouts: whether each lane k < K holds a row
+// (`slot` >= 0) exactly when expert id `e` is valid and not named by a lower
+// lane (lanes >= K hold e = -1).  Detects a layout of another routing.
+__device__ __forceinline__ bool choices_agree(int64_t e, int E, int K, int slot, int lane) {
+  const uint32_t peers = __match_any_sync(0xffffffffu, (unsigned long long)e);
+  const bool first = e >= 0 && e < E && (peers & ((1u << lane) - 1u)) == 0u;
+  const bool ok = lane >= K || first == (slot >= 0);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -37,9 +37,13 @@ constexpr bool kFp8WarpSpecialised = true;
 struct DispatchParams {
   const uint16_t *x;
   int T, H, K, E, R, epr, groups;
+  int D;          // destinations per token: R ranks, or K experts (expanded)
+  bool expanded;  // token_slot is [T * K]: one row per (token, expert)
+  const int32_t *xoff, *xrows;  // expanded: segment starts [E+1], rows [E]
+  bool zero_padding;            // expanded: write the padding rows
   const int64_t *topk_idx;
   const float *topk_weights;
-  const int32_t *token_slot;
+  const int32_t *token_slot;    // [T * D]
   uint32_t *error_word;
   void *recv_x;
   float *recv_x_scales;
@@ -66,16 +70,38 @@ __device__ __forceinline__ void issue_row_load(const DispatchParams &p, unsigned
                  &full[s], policy);
 }
 
-// Cumulative recv stats: lane k < K adds one to its expert's count when the
-// row of the expert's rank was received (slot in [0, cap)).  Warp-collective.
+// Warp-collective: the layout holds exactly the rows this routing needs
+// (slot_lo / slot_hi: the slots of destinations lane and lane + 32; e: the
+// expert of slot k = lane, -1 past K).
+__device__ __forceinline__ bool layout_agrees(const DispatchParams &p, int64_t e, int slot_lo, int slot_hi,
+                                              int lane) {
+  return p.expanded ? choices_agree(e, p.E, p.K, slot_lo, lane)
+                    : ranks_agree(e, p.E, p.epr, p.R, slot_lo, slot_hi, lane);
+}
+
+// Cumulative recv stats: lane k < K adds one to its expert's count when that
+// expert's row (the rank's row, or the expanded row of slot k) was received
+// (slot in [0, cap)).  Warp-collective.
 __device__ __forceinline__ void count_received(const DispatchParams &p, int64_t e, int slot_lo, int slot_hi,
                                                int lane) {
   const bool valid = e >= 0 && e < p.E;
   const int r = valid ? static_cast<int>(e) / p.epr : 0;
   const int s_lo = __shfl_sync(0xffffffffu, slot_lo, r & (kWarpSize - 1));
   const int s_hi = __shfl_sync(0xffffffffu, slot_hi, r & (kWarpSize - 1));
-  const int slot = r < kWarpSize ? s_lo : s_hi;
+  const int slot = p.expanded ? slot_lo : (r < kWarpSize ? s_lo : s_hi);
   if (valid && slot >= 0 && slot < p.cap) atomicAdd(p.stats + e, 1u);
+}
+
+// Whether top-k slot k (expert e) is marked in the received row of
+// destination j, and the local expert id written there: a rank row marks
+// every expert of its rank; an expanded row marks only its own slot (TileScale
+// PR #68, commit message on the expanded combine).
+__device__ __forceinline__ bool marks(const DispatchParams &p, int64_t e, int k, int j) {
+  if (e < 0 || e >= p.E) return false;
+  return p.expanded ? k == j : static_cast<int>(e) / p.epr == j;
+}
+__device__ __forceinline__ int local_expert(const DispatchParams &p, int64_t e) {
+  return static_cast<int>(e) - (static_cast<int>(e) / p.epr) * p.epr;
 }
 
 // Received metadata of token t, by threads [32, blockDim): source token,
@@ -89,37 +115,34 @@ __device__ __forceinline__ void write_metadata(const DispatchParams &p, int t,
   if (threadIdx.x / kWarpSize == 1) {  // warp 1 checks the layout against the routing
     const int lane = threadIdx.x & (kWarpSize - 1);
     const int64_t e = lane < p.K ? __ldg(p.topk_idx + (size_t)t * p.K + lane) : -1;
-    const int lo = lane < p.R ? slots[lane] : -1;
-    const int hi = lane + kWarpSize < p.R ? slots[lane + kWarpSize] : -1;
-    if (!ranks_agree(e, p.E, p.epr, p.R, lo, hi, lane) && lane == 0)
-      set_error(p.error_word, EP_ERRBIT_STALE_LAYOUT);
+    const int lo = lane < p.D ? slots[lane] : -1;
+    const int hi = lane + kWarpSize < p.D ? slots[lane + kWarpSize] : -1;
+    if (!layout_agrees(p, e, lo, hi, lane) && lane == 0) set_error(p.error_word, EP_ERRBIT_STALE_LAYOUT);
     if (p.stats != nullptr) count_received(p, e, lo, hi, lane);
   }
   if (p.recv_src_idx != nullptr) {
-    for (int j = mt; j < p.R; j += nt) {
+    for (int j = mt; j < p.D; j += nt) {
       const int slot = slots[j];
       if (slot >= 0 && slot < p.cap) p.recv_src_idx[slot] = t;
     }
   }
   if (p.recv_topk_idx != nullptr || p.recv_topk_weights != nullptr) {
-    const int RK = p.R * p.K;
-    for (int q = mt; q < RK; q += nt) {
+    const int DK = p.D * p.K;
+    for (int q = mt; q < DK; q += nt) {
       const int j = q / p.K;
       const int k = q - j * p.K;
       const int slot = slots[j];
       if (slot < 0 || slot >= p.cap) continue;
       const int64_t e = __ldg(p.topk_idx + (size_t)t * p.K + k);
-      const bool here = e >= 0 && e < p.E && static_cast<int>(e) / p.epr == j;
-      if (p.recv_topk_idx != nullptr)
-        p.recv_topk_idx[(size_t)slot * p.K + k] = here ? static_cast<int>(e) - j * p.epr : -1;
+      const bool here = marks(p, e, k, j);
+      if (p.recv_topk_idx != nullptr) p.recv_topk_idx[(size_t)slot * p.K + k] = here ? local_expert(p, e) : -1;
       if (p.recv_topk_weights != nullptr)
-        p.recv_topk_weights[(size_t)slot * p.K + k] =
-            here ? __ldg(p.topk_weights + (size_t)t * p.K + k) : 0.0f;
+        p.recv_topk_weights[(size_t)slot * p.K + k] = here ? __ldg(p.topk_weights + (size_t)t * p.K + k) : 0.0f;
     }
   }
   if constexpr (FP8) {
-    const int RG = p.R * p.groups;
-    for (int q = mt; q < RG; q += nt) {
+    const int DG = p.D * p.groups;
+    for (int q = mt; q < DG; q += nt) {
       const int j = q / p.groups;
       const int g = q - j * p.groups;
       const int slot = slots[j];
@@ -187,7 +210,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(Dispatc
     int32_t *slots = s_slot + b * EP_MAX_RANKS;
     unsigned char *stage = stages + (size_t)s * p.stage_stride;
 
-    if (tid < p.R) slots[tid] = __ldg(p.token_slot + (size_t)t * p.R + tid);
+    if (tid < p.D) slots[tid] = __ldg(p.token_slot + (size_t)t * p.D + tid);
     if constexpr (FP8) {
       // the stores of token i-2 read obuf[b]: let them finish reading it
       if (warp == 0) bulk_wait_read<1>();
@@ -213,7 +236,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(Dispatc
       if (*s_abort) break;
       if (warp == 0) {
         if (lane == 0 && i + S < n) issue_row_load(p, stages, full, loads_issued++, policy);
-        for (int j = lane; j < p.R; j += kWarpSize) {
+        for (int j = lane; j < p.D; j += kWarpSize) {
           const int slot = slots[j];
           if (slot < 0) continue;
           if (slot < p.cap)
@@ -235,7 +258,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(Dispatc
             set_error(p.error_word, EP_ERRBIT_TIMEOUT);
           }
         } else {
-          for (int j = lane; j < p.R; j += kWarpSize) {
+          for (int j = lane; j < p.D; j += kWarpSize) {
             const int slot = slots[j];
             if (slot < 0) continue;
             if (slot < p.cap)
@@ -350,11 +373,11 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
     for (int i = 0; i < n && !*s_abort; ++i) {
       const int t = blockIdx.x + i * gridDim.x;
       const int o = i % kWsOut;
-      const int32_t *srow = p.token_slot + (size_t)t * p.R;
-      int slot_lo = lane < p.R ? __ldg(srow + lane) : -1;
-      int slot_hi = lane + kWarpSize < p.R ? __ldg(srow + lane + kWarpSize) : -1;
+      const int32_t *srow = p.token_slot + (size_t)t * p.D;
+      int slot_lo = lane < p.D ? __ldg(srow + lane) : -1;
+      int slot_hi = lane + kWarpSize < p.D ? __ldg(srow + lane + kWarpSize) : -1;
       const int64_t e = lane < p.K ? __ldg(p.topk_idx + (size_t)t * p.K + lane) : -1;
-      if (!ranks_agree(e, p.E, p.epr, p.R, slot_lo, slot_hi, lane) && lane == 0)
+      if (!layout_agrees(p, e, slot_lo, slot_hi, lane) && lane == 0)
         set_error(p.error_word, EP_ERRBIT_STALE_LAYOUT);
       if (slot_lo >= p.cap) {
         set_error(p.error_word, EP_ERRBIT_CAPACITY);
@@ -368,14 +391,14 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
       const float w = (lane < p.K && p.recv_topk_weights != nullptr)
                           ? __ldg(p.topk_weights + (size_t)t * p.K + lane) : 0.0f;
       // received metadata: needs no shared memory, runs ahead of the cast
-      for (int r = 0; r < p.R; ++r) {
+      for (int r = 0; r < p.D; ++r) {
         const int slot = __shfl_sync(0xffffffffu, r < kWarpSize ? slot_lo : slot_hi, r & (kWarpSize - 1));
         if (slot < 0) continue;
         if (lane == 0 && p.recv_src_idx != nullptr) p.recv_src_idx[slot] = t;
         if (lane < p.K) {
-          const bool here = e >= 0 && e < p.E && static_cast<int>(e) / p.epr == r;
+          const bool here = marks(p, e, lane, r);
           if (p.recv_topk_idx != nullptr)
-            p.recv_topk_idx[(size_t)slot * p.K + lane] = here ? static_cast<int>(e) - r * p.epr : -1;
+            p.recv_topk_idx[(size_t)slot * p.K + lane] = here ? local_expert(p, e) : -1;
           if (p.recv_topk_weights != nullptr) p.recv_topk_weights[(size_t)slot * p.K + lane] = here ? w : 0.0f;
         }
       }
@@ -413,9 +436,9 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
       bulk_commit();
       if (!scale_bulk) {
         s_slot[lane] = slot_lo;
-        if (p.R > kWarpSize) s_slot[lane + kWarpSize] = slot_hi;
+        if (p.D > kWarpSize) s_slot[lane + kWarpSize] = slot_hi;
         __syncwarp();
-        const int RG = p.R * p.groups;
+        const int RG = p.D * p.groups;
         for (int q = lane; q < RG; q += kWarpSize) {
           const int r = q / p.groups;
           const int g = q - r * p.groups;
@@ -502,6 +525,46 @@ ep_status_t launch_ws(DispatchParams &p, const DeviceInfo &di, cudaStream_t stre
 }
 
 
+// ------------------------------------------------------------------------
+// Padding rows of an expanded layout (zero_padding): each expert's rows past
+// its last selection, up to the aligned end of its segment, get a zero
+// payload (and zero scales), source -1, all top-k slots -1 and weights 0.
+// A block per expert (grid-stride).
+
+constexpr int kPadThreads = 256;
+
+__global__ void __launch_bounds__(kPadThreads) pad_kernel(DispatchParams p) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int4 zero = make_int4(0, 0, 0, 0);
+  for (int e = blockIdx.x; e < p.E; e += gridDim.x) {
+    const int s0 = __ldg(p.xoff + e) + __ldg(p.xrows + e);
+    const int s1 = __ldg(p.xoff + e + 1);
+    for (int s = s0; s < s1; ++s) {
+      if (s >= p.cap) {
+        if (threadIdx.x == 0) set_error(p.error_word, EP_ERRBIT_CAPACITY);
+        continue;
+      }
+      int4 *row = reinterpret_cast<int4 *>(static_cast<unsigned char *>(p.recv_x) + (size_t)s * p.row_out_bytes);
+      for (uint32_t i = threadIdx.x; i < p.row_out_bytes / 16; i += kPadThreads) row[i] = zero;
+      if (p.groups > 0 && !p.packed)
+        for (int g = threadIdx.x; g < p.groups; g += kPadThreads) p.recv_x_scales[(size_t)s * p.groups + g] = 0.0f;
+      if (threadIdx.x == 0 && p.recv_src_idx != nullptr) p.recv_src_idx[s] = -1;
+      if ((int)threadIdx.x < p.K) {
+        if (p.recv_topk_idx != nullptr) p.recv_topk_idx[(size_t)s * p.K + threadIdx.x] = -1;
+        if (p.recv_topk_weights != nullptr) p.recv_topk_weights[(size_t)s * p.K + threadIdx.x] = 0.0f;
+      }
+    }
+  }
+}
+
+ep_status_t launch_pad(const DispatchParams &p, const DeviceInfo &di, cudaStream_t stream) {
+  const int grid = std::min(p.E, 2 * di.num_sms);
+  cudaError_t e = launch_kernel(pad_kernel, grid, kPadThreads, 0, stream, false, p);
+  if (e != cudaSuccess) return cuda_fail(e, "launch pad_kernel");
+  return EP_OK;
+}
+
 size_t dispatch_smem_bytes(const DispatchParams &p, bool fp8) {
   size_t bytes = kHeaderBytes + (size_t)p.stages * p.stage_stride;
   if (fp8) bytes += 2 * (size_t)p.out_stride + 2 * (size_t)p.scale_stride;
@@ -541,10 +604,16 @@ ep_status_t launch_ring(DispatchParams &p, const DeviceInfo &di, cudaStream_t st
 }  // namespace
 
 ep_status_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream) {
-  if (a.num_tokens == 0) return EP_OK;
+  const bool pad = a.expanded && a.zero_padding;
+  if (a.num_tokens == 0 && !pad) return EP_OK;
   const DeviceInfo *di = current_device_info();
   if (di == nullptr) return EP_ERR_CUDA;
   DispatchParams p = {};
+  p.D = a.expanded ? a.num_topk : a.num_ranks;
+  p.expanded = a.expanded;
+  p.xoff = a.expert_offset;
+  p.xrows = a.num_rows_per_expert;
+  p.zero_padding = a.zero_padding;
   p.x = a.x;
   p.T = a.num_tokens;
   p.H = a.hidden;
@@ -570,9 +639,16 @@ ep_status_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream) {
   p.stage_stride = (p.row_in_bytes + 127u) / 128u * 128u;
   p.out_stride = a.fp8 ? (p.row_out_bytes + 127u) / 128u * 128u : 0u;
   p.scale_stride = (a.fp8 && !p.packed) ? ((uint32_t)p.groups * 4u + 15u) / 16u * 16u : 0u;
-  // packed rows are only built by the warp-specialised kernel
-  if (a.fp8) return (kFp8WarpSpecialised || p.packed) ? launch_ws(p, *di, stream) : launch_ring<true>(p, *di, stream);
-  return launch_ring<false>(p, *di, stream);
+  ep_status_t st = EP_OK;
+  if (a.num_tokens > 0) {
+    // packed rows are only built by the warp-specialised kernel
+    if (a.fp8)
+      st = (kFp8WarpSpecialised || p.packed) ? launch_ws(p, *di, stream) : launch_ring<true>(p, *di, stream);
+    else
+      st = launch_ring<false>(p, *di, stream);
+  }
+  if (st == EP_OK && pad) st = launch_pad(p, *di, stream);
+  return st;
 }
 
 }  // namespace ep

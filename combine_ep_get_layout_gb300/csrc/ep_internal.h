@@ -38,6 +38,12 @@ ep_status_t launch_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
                           int num_ranks, const ep_layout_t &layout, void *workspace,
                           cudaStream_t stream);
 
+// ---- expanded layout (ep_layout_expanded.cu)
+size_t expanded_layout_workspace_bytes(int num_tokens, int num_experts);
+ep_status_t launch_layout_expanded(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
+                                   int expert_alignment, const ep_expanded_layout_t &layout, void *workspace,
+                                   cudaStream_t stream);
+
 // ---- dispatch (ep_dispatch.cu)
 // Bytes of a packed fp8 row: codes, scales, zero padding to 16 bytes, or to
 // 512 when that adds under 5% to the unpadded row.
@@ -53,8 +59,12 @@ struct DispatchArgs {
   int num_tokens, hidden, num_topk, num_experts, num_ranks;
   const int64_t *topk_idx;
   const float *topk_weights;
-  const int32_t *token_slot;
+  const int32_t *token_slot;  // [T * D]: rank layout D = R, expanded D = K
   uint32_t *error_word;
+  bool expanded;
+  const int32_t *expert_offset;        // expanded: [E+1]
+  const int32_t *num_rows_per_expert;  // expanded: [E]
+  bool zero_padding;                   // expanded: write the padding rows
   bool fp8;
   int packed_row_bytes;  // > 0: packed fp8 rows of this many bytes
   void *recv_x;
@@ -71,6 +81,7 @@ ep_status_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream);
 struct CombineArgs {
   const uint16_t *y;
   int recv_capacity, hidden, num_tokens, num_ranks, num_topk, num_experts;
+  bool expanded;              // token_slot is [T * K] of an expanded layout
   const int32_t *token_slot;
   uint32_t *error_word;
   const int64_t *topk_idx;

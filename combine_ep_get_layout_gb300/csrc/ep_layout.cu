@@ -29,24 +29,19 @@ constexpr int kLayoutThreads = 256;  // one token per thread per chunk
 constexpr int kLayoutWarps = kLayoutThreads / kWarpSize;
 constexpr size_t kPartialOffset = 256;  // bytes: barrier words come first
 
-struct BarrierWords {
-  uint32_t arrive;
-  uint32_t depart;
-};
-
 struct LayoutParams {
   const int64_t *topk_idx;
   int num_tokens, num_topk, num_experts, num_ranks, experts_per_rank;
   int tokens_per_block;
   ep_layout_t out;
-  BarrierWords *bar;
+  GridBarrierWords *bar;
   int32_t *partial;  // [gridDim.x * R] per-block, per-rank token counts
 };
 
 size_t layout_smem_bytes(int tokens_per_block, int E, int R) {
   // masks[tpb] u64, hist[E], blk_cnt[R], warp_off[W*R], chunk_tot[R],
   // tot[R], before[R], base[R+1], run[R], flags[2], scan_all[T], scan_before[T]
-  size_t ints = (size_t)E + R + (size_t)kLayoutWarps * R + R + R + R + (R + 1) + R + 2 + 2 * kLayoutThreads;
+  size_t ints = (size_t)E + R + (size_t)kLayoutWarps * R + R + R + R + (R + 1) + R + 3 + 2 * kLayoutThreads;
   return (size_t)tokens_per_block * sizeof(uint64_t) + ints * sizeof(int32_t);
 }
 
@@ -71,8 +66,8 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutParams p) 
   int *before = tot + R;
   int *base = before + R;  // [R + 1]
   int *run = base + R + 1;
-  int *flags = run + R;  // [0] bad index seen, [1] barrier timed out
-  int *scan_all = flags + 2;                  // [kLayoutThreads]
+  int *flags = run + R;  // [0] bad index seen, [1] barrier timed out, [2] barrier scratch
+  int *scan_all = flags + 3;                  // [kLayoutThreads]
   int *scan_before = scan_all + kLayoutThreads;  // [kLayoutThreads]
 
   for (int i = tid; i < E; i += kLayoutThreads) hist[i] = 0;
@@ -125,20 +120,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutParams p) 
 
   // ---- exchange: bounded grid barrier (all blocks co-resident)
   __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    atomicAdd(&p.bar->arrive, 1u);
-    const uint64_t t0 = global_timer_ns();
-    while (ld_acquire_gpu(&p.bar->arrive) < static_cast<uint32_t>(G)) {
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        flags[1] = 1;
-        break;
-      }
-      __nanosleep(32);
-    }
-    __threadfence();
-  }
-  __syncthreads();
+  if (!grid_barrier(p.bar, &flags[2]) && tid == 0) flags[1] = 1;
 
   // ---- phase 2: bases (exclusive scan over ranks and over earlier blocks);
   // the block totals are summed by kLayoutThreads / R threads per rank
@@ -244,13 +226,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutParams p) 
   }
 
   // ---- exit: the last block out resets the barrier words for the next call
-  if (tid == 0) {
-    const uint32_t prev = atomicAdd(&p.bar->depart, 1u);
-    if (prev == static_cast<uint32_t>(G) - 1u) {
-      atomicExch(&p.bar->arrive, 0u);
-      atomicExch(&p.bar->depart, 0u);
-    }
-  }
+  grid_barrier_exit(p.bar);
 }
 
 int max_layout_blocks(int num_tokens) {
@@ -315,7 +291,7 @@ ep_status_t launch_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
   p.experts_per_rank = num_experts / num_ranks;
   p.tokens_per_block = (num_tokens + grid - 1) / grid;
   p.out = layout;
-  p.bar = static_cast<BarrierWords *>(workspace);
+  p.bar = static_cast<GridBarrierWords *>(workspace);
   p.partial = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(workspace) + kPartialOffset);
 
   cudaError_t e = launch_kernel(kernel, grid, kLayoutThreads, smem, stream, true, p);

@@ -67,6 +67,8 @@ typedef enum {
 #define EP_ERRBIT_TIMEOUT 0x4u    /* a bounded device wait gave up           */
 #define EP_ERRBIT_STALE_LAYOUT 0x8u /* routing and layout disagree on a token's
                                        set of ranks (a layout of another routing) */
+#define EP_ERRBIT_DUP_EXPERT 0x10u  /* expanded layout: a token names an expert
+                                       twice; the repeat gets no row           */
 
 /* Limits of this implementation (EP_ERR_UNSUPPORTED beyond them). */
 #define EP_MAX_RANKS 64
@@ -319,6 +321,112 @@ typedef struct {
     void *out;
 } ep_combine_args_t;
 ep_status_t ep_combine_ex(const ep_combine_args_t *args, ep_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* Expanded (per-expert) layout                                        */
+/* ------------------------------------------------------------------ */
+
+/*
+ * The expanded layout of one routing: one received row per (token, expert)
+ * selection instead of per (token, rank), rows grouped by expert so that
+ * each expert's rows form the contiguous block a grouped GEMM consumes, each
+ * block rounded up to expert_alignment rows (TileScale PR #68, commit
+ * message on do_expand).  Experts are contiguous per rank, so the rows are
+ * rank-major too: rank r's rows are
+ * [expert_offset[r*E/R], expert_offset[(r+1)*E/R]).  Caller-allocated:
+ *   num_rows_per_expert [E]   int32: rows of each expert.
+ *   expert_offset       [E+1] int32: first row of each expert's block (the
+ *                             exclusive prefix sum of rows rounded up to the
+ *                             alignment); expert_offset[E] is the number of
+ *                             rows including padding.
+ *   token_slot          [T*K] int32: the row of (t, k), or -1 (no
+ *                             selection, an invalid id, or a repeat of an
+ *                             expert already named by t).  Inside a block
+ *                             rows are in ascending (token, k) order.
+ *   error_word          [1]   uint32: EP_ERRBIT_* (cleared by the layout).
+ */
+typedef struct {
+    int32_t *num_rows_per_expert;
+    int32_t *expert_offset;
+    int32_t *token_slot;
+    uint32_t *error_word;
+} ep_expanded_layout_t;
+
+/* Workspace bytes of ep_get_layout_expanded (zero-filled once at
+ * allocation, left zeroed by every call, reusable for smaller sizes). */
+size_t ep_expanded_layout_workspace_bytes(int num_tokens, int num_experts);
+
+/*
+ * The expanded layout: phase 1 tallies rows per expert, phase 2 turns the
+ * tallies into aligned segment starts, phase 3 adds each row's rank in its
+ * segment -- the do_expand generalisation of the count / exchange / scatter
+ * phases with the destination redefined from rank to expert (TileScale PR
+ * #68, commit message on do_expand).  One cooperative kernel with a bounded
+ * grid barrier.  1 <= expert_alignment <= 4096; limits as ep_get_layout;
+ * token_slot 16-byte aligned.
+ */
+ep_status_t ep_get_layout_expanded(const int64_t *topk_idx, int num_tokens, int num_topk,
+                                   int num_experts, int expert_alignment,
+                                   const ep_expanded_layout_t *layout, void *workspace,
+                                   size_t workspace_bytes, ep_stream_t stream);
+
+/*
+ * Expanded dispatch: row token_slot[t][k] receives x[t] (bf16, fp8 + scales,
+ * or packed fp8), recv_src_idx = t, and recv_topk_idx / recv_topk_weights
+ * mark only slot k -- the row's own expert as a local id, and its weight --
+ * with -1 / 0 elsewhere (same page: an expanded row marks only the expert it
+ * belongs to).  zero_padding != 0: the padding rows of every block are
+ * written as zeros (payload and scales), source -1, all top-k slots -1 and
+ * weights 0 (zero_padding clears the gap).  Rows at or past recv_capacity
+ * are skipped with EP_ERRBIT_CAPACITY; expert_offset[E] rows always suffice.
+ * cumulative_recv_stats counts each written row for its expert.  Members
+ * otherwise as ep_dispatch_args_t; num_ranks gives the local ids.
+ */
+typedef struct {
+    const void *x;
+    int num_tokens;
+    int hidden;
+    const int64_t *topk_idx;
+    const float *topk_weights;
+    int num_topk;
+    int num_experts;
+    int num_ranks;
+    const ep_expanded_layout_t *layout;
+    ep_dtype_t dtype;
+    void *recv_x;
+    float *recv_x_scales;
+    int32_t *recv_src_idx;
+    int32_t *recv_topk_idx;
+    float *recv_topk_weights;
+    int recv_capacity;
+    int zero_padding;
+    uint32_t *cumulative_recv_stats;
+} ep_dispatch_expanded_args_t;
+ep_status_t ep_dispatch_expanded(const ep_dispatch_expanded_args_t *args, ep_stream_t stream);
+
+/*
+ * Expanded combine: out[t] = bf16(bias0 + bias1 + the sum, in ascending row
+ * order, of c * y[row] over t's rows), fp32 with separate multiply and add;
+ * c is the row's own gate weight (topk_weights given) or 1.  This is
+ * DeepEP's kDoExpandedSend -- a token's rows summed before the rank reduce
+ * (same page, commit message on the expanded combine) -- on one GPU.
+ * y has recv_capacity rows indexed like the dispatched rows.
+ */
+typedef struct {
+    const void *y;
+    int recv_capacity;
+    int hidden;
+    const ep_expanded_layout_t *layout;
+    int num_tokens;
+    int num_topk;
+    const int64_t *topk_idx;
+    const float *topk_weights;
+    int num_experts;
+    const void *bias0;
+    const void *bias1;
+    void *out;
+} ep_combine_expanded_args_t;
+ep_status_t ep_combine_expanded(const ep_combine_expanded_args_t *args, ep_stream_t stream);
 
 /* A static, human-readable name of a status. */
 const char *ep_status_str(ep_status_t status);

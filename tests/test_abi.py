@@ -193,3 +193,104 @@ def test_combine_ex_rejects_misaligned_bias(lib):
                             0x20008, None, 0x20000)
     name, msg = _status(lib, lib.ep_combine_ex(C.byref(a), None))
     assert name == "EP_ERR_INVALID_ARG" and "bias0" in msg
+
+
+def _xlayout(base=0x10000):
+    from combine_ep_get_layout_gb300._native import ep_expanded_layout_t
+    return ep_expanded_layout_t(base, base + 0x100, base + 0x200, base + 0x400)
+
+
+def test_expanded_workspace_bytes(lib):
+    a = lib.ep_expanded_layout_workspace_bytes(8192, 256)
+    assert a > 0 and a % 256 == 0
+    assert lib.ep_expanded_layout_workspace_bytes(65536, 256) > a
+    assert lib.ep_expanded_layout_workspace_bytes(0, 16) > 0
+    assert lib.ep_expanded_layout_workspace_bytes(-1, 16) == 0
+    assert lib.ep_expanded_layout_workspace_bytes(10, 0) == 0
+    assert lib.ep_expanded_layout_workspace_bytes(10, 4097) == 0
+
+
+@pytest.mark.parametrize("kw,needle,status", [
+    (dict(T=-1), "num_tokens", "EP_ERR_INVALID_ARG"),
+    (dict(K=0), "num_topk", "EP_ERR_INVALID_ARG"),
+    (dict(K=33), "num_topk", "EP_ERR_UNSUPPORTED"),
+    (dict(E=0), "num_experts", "EP_ERR_INVALID_ARG"),
+    (dict(E=4097), "num_experts", "EP_ERR_UNSUPPORTED"),
+    (dict(align=0), "expert_alignment", "EP_ERR_INVALID_ARG"),
+    (dict(align=4097), "expert_alignment", "EP_ERR_INVALID_ARG"),
+    (dict(idx=None), "topk_idx is NULL", "EP_ERR_INVALID_ARG"),
+    (dict(idx=C.c_void_p(0x20004)), "aligned", "EP_ERR_INVALID_ARG"),
+    (dict(layout_none=True), "layout is NULL", "EP_ERR_INVALID_ARG"),
+    (dict(ws=None), "workspace is NULL", "EP_ERR_INVALID_ARG"),
+    (dict(ws_bytes=16), "workspace_bytes", "EP_ERR_INVALID_ARG"),
+])
+def test_get_layout_expanded_rejects(lib, kw, needle, status):
+    a = dict(idx=FAKE, T=100, K=4, E=16, align=8, ws=FAKE, ws_bytes=1 << 20, layout_none=False)
+    a.update(kw)
+    lay = None if a["layout_none"] else C.byref(_xlayout())
+    s = lib.ep_get_layout_expanded(a["idx"], a["T"], a["K"], a["E"], a["align"], lay, a["ws"],
+                                   a["ws_bytes"], None)
+    name, msg = _status(lib, s)
+    assert name == status, (name, msg)
+    assert needle in msg
+
+
+def _xdargs(**kw):
+    from combine_ep_get_layout_gb300 import _native as N
+    lay = kw.pop("lay", _xlayout())
+    a = dict(x=0x20000, num_tokens=100, hidden=256, topk_idx=0x20000, topk_weights=0x20000,
+             num_topk=4, num_experts=16, num_ranks=4, layout=C.pointer(lay), dtype=0,
+             recv_x=0x20000, recv_x_scales=0x20000, recv_src_idx=None, recv_topk_idx=None,
+             recv_topk_weights=None, recv_capacity=400, zero_padding=1, cumulative_recv_stats=None)
+    a.update(kw)
+    return N.ep_dispatch_expanded_args_t(**a), lay
+
+
+@pytest.mark.parametrize("kw,needle", [
+    (dict(dtype=5), "dtype"),
+    (dict(dtype=1, hidden=264), "multiple of 128"),
+    (dict(hidden=12), "multiple of 8"),
+    (dict(recv_capacity=-1), "recv_capacity"),
+    (dict(x=0x20004), "x is not 16-byte aligned"),
+    (dict(recv_x=None), "recv_x is NULL"),
+    (dict(dtype=1, recv_x_scales=None), "recv_x_scales is NULL"),
+    (dict(recv_topk_weights=0x20000, topk_weights=None), "topk_weights is NULL"),
+    (dict(cumulative_recv_stats=0x20001), "cumulative_recv_stats"),
+    (dict(num_experts=10), "multiple"),
+])
+def test_dispatch_expanded_rejects(lib, kw, needle):
+    a, _keep = _xdargs(**kw)
+    name, msg = _status(lib, lib.ep_dispatch_expanded(C.byref(a), None))
+    assert name == "EP_ERR_INVALID_ARG", (name, msg)
+    assert needle in msg
+    assert _status(lib, lib.ep_dispatch_expanded(None, None))[0] == "EP_ERR_INVALID_ARG"
+
+
+def test_dispatch_expanded_zero_padding_needs_offsets(lib):
+    from combine_ep_get_layout_gb300._native import ep_expanded_layout_t
+    lay = ep_expanded_layout_t(0x10000, None, 0x10200, 0x10400)
+    a, _keep = _xdargs(lay=lay)
+    name, msg = _status(lib, lib.ep_dispatch_expanded(C.byref(a), None))
+    assert name == "EP_ERR_INVALID_ARG" and "expert_offset" in msg
+
+
+@pytest.mark.parametrize("kw,needle", [
+    (dict(idx=None), "both"),
+    (dict(H=12), "multiple of 8"),
+    (dict(K=0), "num_topk"),
+    (dict(E=0), "num_experts"),
+    (dict(out=None), "out is NULL"),
+    (dict(y=0x20004), "y is not 16-byte aligned"),
+    (dict(b1=0x20008), "bias1"),
+])
+def test_combine_expanded_rejects(lib, kw, needle):
+    from combine_ep_get_layout_gb300 import _native as N
+    a = dict(y=0x20000, cap=400, H=256, T=100, K=4, idx=0x20000, w=0x20000, E=16, b0=None, b1=None,
+             out=0x20000)
+    a.update(kw)
+    lay = _xlayout()
+    args = N.ep_combine_expanded_args_t(a["y"], a["cap"], a["H"], C.pointer(lay), a["T"], a["K"],
+                                        a["idx"], a["w"], a["E"], a["b0"], a["b1"], a["out"])
+    name, msg = _status(lib, lib.ep_combine_expanded(C.byref(args), None))
+    assert name == "EP_ERR_INVALID_ARG", (name, msg)
+    assert needle in msg
