@@ -95,9 +95,11 @@ class Layout:
     num_tokens: int
     num_experts: int
     num_ranks: int
+    work_counters: Optional[torch.Tensor] = None  # int32 [4]: blocks draw tokens from a counter
 
     @staticmethod
-    def empty(num_tokens: int, num_experts: int, num_ranks: int, device) -> "Layout":
+    def empty(num_tokens: int, num_experts: int, num_ranks: int, device,
+              work_counters: bool = True) -> "Layout":
         dev = torch.device(device)
         i32 = dict(dtype=torch.int32, device=dev)
         ws = ep_layout_workspace_bytes(num_tokens, num_experts, num_ranks)
@@ -108,13 +110,15 @@ class Layout:
             torch.empty((num_tokens, num_ranks), **i32),
             torch.zeros(1, **i32),
             torch.zeros(max(ws, 16), dtype=torch.uint8, device=dev),
-            num_tokens, num_experts, num_ranks)
+            num_tokens, num_experts, num_ranks,
+            torch.zeros(N.EP_WORK_COUNTER_WORDS, **i32) if work_counters else None)
 
     def c_struct(self) -> N.ep_layout_t:
         return N.ep_layout_t(
             self.num_tokens_per_expert.data_ptr(), self.num_tokens_per_rank.data_ptr(),
             self.rank_prefix.data_ptr(), self.is_token_in_rank.data_ptr(),
-            self.token_slot.data_ptr(), self.error_word.data_ptr())
+            self.token_slot.data_ptr(), self.error_word.data_ptr(),
+            None if self.work_counters is None else self.work_counters.data_ptr())
 
     def num_recv(self) -> int:
         """N, read back to the host (synchronises)."""
@@ -126,12 +130,16 @@ class Layout:
 
 
 def ep_get_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int,
-                  layout: Optional[Layout] = None, stream=None) -> Layout:
+                  layout: Optional[Layout] = None, stream=None,
+                  work_counters: bool = True) -> Layout:
+    """The layout of one routing.  A new layout carries work counters
+    unless ``work_counters`` is false (then dispatch and combine give each
+    thread block a fixed stripe of tokens)."""
     _want(topk_idx, "topk_idx", torch.int64)
     T, K = topk_idx.shape
     dev = topk_idx.device
     if layout is None:
-        layout = Layout.empty(T, num_experts, num_ranks, dev)
+        layout = Layout.empty(T, num_experts, num_ranks, dev, work_counters)
     elif (layout.num_tokens, layout.num_experts, layout.num_ranks) != (T, num_experts, num_ranks):
         raise ValueError("layout was allocated for other sizes")
     st = layout.c_struct()
@@ -316,10 +324,11 @@ class ExpandedLayout:
     num_topk: int
     num_experts: int
     expert_alignment: int
+    work_counters: Optional[torch.Tensor] = None  # int32 [4]: blocks draw tokens from a counter
 
     @staticmethod
     def empty(num_tokens: int, num_topk: int, num_experts: int, expert_alignment: int,
-              device) -> "ExpandedLayout":
+              device, work_counters: bool = True) -> "ExpandedLayout":
         dev = torch.device(device)
         i32 = dict(dtype=torch.int32, device=dev)
         ws = ep_expanded_layout_workspace_bytes(num_tokens, num_experts)
@@ -327,12 +336,14 @@ class ExpandedLayout:
             torch.empty(num_experts, **i32), torch.empty(num_experts + 1, **i32),
             torch.empty((num_tokens, num_topk), **i32), torch.zeros(1, **i32),
             torch.zeros(max(ws, 16), dtype=torch.uint8, device=dev),
-            num_tokens, num_topk, num_experts, expert_alignment)
+            num_tokens, num_topk, num_experts, expert_alignment,
+            torch.zeros(N.EP_WORK_COUNTER_WORDS, **i32) if work_counters else None)
 
     def c_struct(self) -> N.ep_expanded_layout_t:
         return N.ep_expanded_layout_t(
             self.num_rows_per_expert.data_ptr(), self.expert_offset.data_ptr(),
-            self.token_slot.data_ptr(), self.error_word.data_ptr())
+            self.token_slot.data_ptr(), self.error_word.data_ptr(),
+            None if self.work_counters is None else self.work_counters.data_ptr())
 
     def num_rows(self) -> int:
         """Rows including padding, read back to the host (synchronises)."""
@@ -347,12 +358,13 @@ class ExpandedLayout:
 
 
 def ep_get_layout_expanded(topk_idx: torch.Tensor, num_experts: int, expert_alignment: int = 1,
-                           layout: Optional[ExpandedLayout] = None, stream=None) -> ExpandedLayout:
+                           layout: Optional[ExpandedLayout] = None, stream=None,
+                           work_counters: bool = True) -> ExpandedLayout:
     _want(topk_idx, "topk_idx", torch.int64)
     T, K = topk_idx.shape
     dev = topk_idx.device
     if layout is None:
-        layout = ExpandedLayout.empty(T, K, num_experts, expert_alignment, dev)
+        layout = ExpandedLayout.empty(T, K, num_experts, expert_alignment, dev, work_counters)
     elif (layout.num_tokens, layout.num_topk, layout.num_experts) != (T, K, num_experts):
         raise ValueError("layout was allocated for other sizes")
     layout.expert_alignment = expert_alignment

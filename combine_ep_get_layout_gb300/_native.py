@@ -33,6 +33,9 @@ EP_MAX_EXPERTS = 4096
 EP_MAX_HIDDEN = 16384
 EP_FP8_GROUP = 128
 EP_NOALLOC_SCRATCH_BYTES = 256 * 1024
+EP_WORK_COUNTER_WORDS = 4
+
+ABI_VERSION = 2  # EP_ABI_VERSION of the header these bindings mirror
 
 
 class ep_layout_t(C.Structure):
@@ -43,6 +46,7 @@ class ep_layout_t(C.Structure):
         ("is_token_in_rank", C.c_void_p),
         ("token_slot", C.c_void_p),
         ("error_word", C.c_void_p),
+        ("work_counters", C.c_void_p),
     ]
 
 
@@ -74,6 +78,7 @@ class ep_expanded_layout_t(C.Structure):
         ("expert_offset", C.c_void_p),
         ("token_slot", C.c_void_p),
         ("error_word", C.c_void_p),
+        ("work_counters", C.c_void_p),
     ]
 
 
@@ -140,7 +145,7 @@ def load():
                 f = getattr(lib, name)
                 f.restype = res
                 f.argtypes = args
-            if lib.ep_abi_version() != 1:
+            if lib.ep_abi_version() != ABI_VERSION:
                 raise RuntimeError("libep_gb300.so ABI version mismatch")
             _lib = lib
     return _lib

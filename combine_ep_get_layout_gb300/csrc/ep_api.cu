@@ -138,6 +138,7 @@ ep_status_t ep_get_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
   EP_CHECK(check_ptr(fn, "layout.is_token_in_rank", layout->is_token_in_rank, 16, any));
   EP_CHECK(check_ptr(fn, "layout.token_slot", layout->token_slot, 16, any));
   EP_CHECK(check_ptr(fn, "layout.error_word", layout->error_word, 4, true));
+  EP_CHECK(check_ptr(fn, "layout.work_counters", layout->work_counters, 16, false));
   EP_CHECK(check_ptr(fn, "workspace", workspace, 16, true));
   const size_t need = layout_workspace_bytes(num_tokens, num_experts, num_ranks);
   if (workspace_bytes < need)
@@ -176,6 +177,7 @@ ep_status_t ep_dispatch_ex(const ep_dispatch_args_t *args, ep_stream_t stream) {
   if (x.layout == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: layout is NULL", fn);
   EP_CHECK(check_ptr(fn, "layout.token_slot", x.layout->token_slot, 4, any));
   EP_CHECK(check_ptr(fn, "layout.error_word", x.layout->error_word, 4, true));
+  EP_CHECK(check_ptr(fn, "layout.work_counters", x.layout->work_counters, 16, false));
   EP_CHECK(check_ptr(fn, "recv_x", x.recv_x, 16, rows));
   EP_CHECK(check_ptr(fn, "recv_x_scales", x.recv_x_scales, 4, fp8 && !packed && rows));
   EP_CHECK(check_ptr(fn, "recv_src_idx", x.recv_src_idx, 4, false));
@@ -200,6 +202,7 @@ ep_status_t ep_dispatch_ex(const ep_dispatch_args_t *args, ep_stream_t stream) {
   a.zero_padding = false;
   a.fp8 = fp8;
   a.packed_row_bytes = packed ? (int)fp8_packed_row_bytes(x.hidden) : 0;
+  a.work_counters = x.layout->work_counters;  // words 0-1: dispatch
   a.recv_x = x.recv_x;
   a.recv_x_scales = packed ? nullptr : x.recv_x_scales;
   a.recv_src_idx = x.recv_src_idx;
@@ -249,6 +252,7 @@ ep_status_t ep_combine_ex(const ep_combine_args_t *args, ep_stream_t stream) {
   if (x.layout == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: layout is NULL", fn);
   EP_CHECK(check_ptr(fn, "layout.token_slot", x.layout->token_slot, 4, any));
   EP_CHECK(check_ptr(fn, "layout.error_word", x.layout->error_word, 4, true));
+  EP_CHECK(check_ptr(fn, "layout.work_counters", x.layout->work_counters, 16, false));
   EP_CHECK(check_ptr(fn, "out", x.out, 16, any));
   EP_CHECK(check_ptr(fn, "bias0", x.bias0, 16, false));
   EP_CHECK(check_ptr(fn, "bias1", x.bias1, 16, false));
@@ -268,6 +272,7 @@ ep_status_t ep_combine_ex(const ep_combine_args_t *args, ep_stream_t stream) {
   a.bias0 = static_cast<const uint16_t *>(x.bias0);
   a.bias1 = static_cast<const uint16_t *>(x.bias1);
   a.out = static_cast<uint16_t *>(x.out);
+  a.work_counters = x.layout->work_counters != nullptr ? x.layout->work_counters + 2 : nullptr;  // words 2-3: combine
   return launch_combine(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -305,6 +310,7 @@ ep_status_t ep_get_layout_expanded(const int64_t *topk_idx, int num_tokens, int 
   EP_CHECK(check_ptr(fn, "layout.expert_offset", layout->expert_offset, 4, true));
   EP_CHECK(check_ptr(fn, "layout.token_slot", layout->token_slot, 16, any));
   EP_CHECK(check_ptr(fn, "layout.error_word", layout->error_word, 4, true));
+  EP_CHECK(check_ptr(fn, "layout.work_counters", layout->work_counters, 16, false));
   EP_CHECK(check_ptr(fn, "workspace", workspace, 16, true));
   const size_t need = expanded_layout_workspace_bytes(num_tokens, num_experts);
   if (workspace_bytes < need)
@@ -338,6 +344,7 @@ ep_status_t ep_dispatch_expanded(const ep_dispatch_expanded_args_t *args, ep_str
   if (x.layout == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: layout is NULL", fn);
   EP_CHECK(check_ptr(fn, "layout.token_slot", x.layout->token_slot, 4, any));
   EP_CHECK(check_ptr(fn, "layout.error_word", x.layout->error_word, 4, true));
+  EP_CHECK(check_ptr(fn, "layout.work_counters", x.layout->work_counters, 16, false));
   EP_CHECK(check_ptr(fn, "layout.expert_offset", x.layout->expert_offset, 4, x.zero_padding != 0));
   EP_CHECK(check_ptr(fn, "layout.num_rows_per_expert", x.layout->num_rows_per_expert, 4, x.zero_padding != 0));
   EP_CHECK(check_ptr(fn, "recv_x", x.recv_x, 16, rows));
@@ -364,6 +371,7 @@ ep_status_t ep_dispatch_expanded(const ep_dispatch_expanded_args_t *args, ep_str
   a.zero_padding = x.zero_padding != 0;
   a.fp8 = fp8;
   a.packed_row_bytes = packed ? (int)fp8_packed_row_bytes(x.hidden) : 0;
+  a.work_counters = x.layout->work_counters;  // words 0-1: dispatch
   a.recv_x = x.recv_x;
   a.recv_x_scales = packed ? nullptr : x.recv_x_scales;
   a.recv_src_idx = x.recv_src_idx;
@@ -402,6 +410,7 @@ ep_status_t ep_combine_expanded(const ep_combine_expanded_args_t *args, ep_strea
   if (x.layout == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: layout is NULL", fn);
   EP_CHECK(check_ptr(fn, "layout.token_slot", x.layout->token_slot, 4, any));
   EP_CHECK(check_ptr(fn, "layout.error_word", x.layout->error_word, 4, true));
+  EP_CHECK(check_ptr(fn, "layout.work_counters", x.layout->work_counters, 16, false));
   EP_CHECK(check_ptr(fn, "out", x.out, 16, any));
   EP_CHECK(check_ptr(fn, "bias0", x.bias0, 16, false));
   EP_CHECK(check_ptr(fn, "bias1", x.bias1, 16, false));
@@ -421,6 +430,7 @@ ep_status_t ep_combine_expanded(const ep_combine_expanded_args_t *args, ep_strea
   a.bias0 = static_cast<const uint16_t *>(x.bias0);
   a.bias1 = static_cast<const uint16_t *>(x.bias1);
   a.out = static_cast<uint16_t *>(x.out);
+  a.work_counters = x.layout->work_counters != nullptr ? x.layout->work_counters + 2 : nullptr;  // words 2-3: combine
   return launch_combine(a, reinterpret_cast<cudaStream_t>(stream));
 }
 

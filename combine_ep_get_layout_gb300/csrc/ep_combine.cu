@@ -37,6 +37,7 @@ struct CombineParams {
   const float *topk_weights;
   const uint16_t *bias0, *bias1;  // [T*H] or null: seed the accumulator
   uint16_t *out;
+  TokenSource tokens;  // the order in which blocks take tokens (warp-specialised kernel)
 };
 
 // acc = bias0 (or 0), then acc = acc + bias1, for 8 consecutive elements.
@@ -228,8 +229,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
 
 // ------------------------------------------------------------------------
 // Warp-specialised kernel (R <= kWsMaxRanks).  A unit is one token's
-// kChunk-element slice of the row; a CTA takes tokens
-// t = blockIdx.x + j * gridDim.x and all units of a token in a row.
+// kChunk-element slice of the row; a CTA takes tokens from its TokenSource
+// (a fixed stripe, or tickets from a grid-wide counter) and all units of a
+// token in a row.  Each unit's stage header carries its token and the
+// CTA's next token (so the reducers can prefetch that token's bias), and a
+// unit with n = -1 ends the CTA's work.
 //   warp 0 (loader)   fetches a token's slots, expert ids and weights one
 //                     token ahead (lanes in parallel), forms each rank's
 //                     coefficient by shuffles, compacts the valid ranks in
@@ -278,9 +282,7 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
   const int tid = threadIdx.x;
   const int warp = tid / kWarpSize;
   const int lane = tid & (kWarpSize - 1);
-  const int nchunk = (p.H + kChunk - 1) / kChunk;
-  // a CTA takes tokens t = blockIdx.x + j * gridDim.x, all chunks of a token in a row
-  const int ntok = p.T > (int)blockIdx.x ? (p.T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int nchunk = (p.H + kChunk - 1) / kChunk;  // a CTA takes all chunks of a token in a row
 
   if (tid == 0) {
     for (int s = 0; s < kCombineStages; ++s) {
@@ -295,14 +297,32 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
   griddep_launch_dependents();
 
   const uint32_t lanes_below = (1u << lane) - 1u;
-  long loads_issued = 0;  // loader lane 0 only
+  long loads_issued = 0;  // loader lane 0: units issued (loads and the end)
   if (warp == 0) {
+    bool drained = false;  // lane 0: no more tokens to draw
+    auto draw = [&](int j) {
+      int t = 0;
+      if (lane == 0) t = draw_token(p.tokens, j, drained);
+      return __shfl_sync(0xffffffffu, t, 0);
+    };
     long i = 0;  // unit counter: stage i % kCombineStages
-    TokenMeta cur = ntok > 0 ? fetch_meta(p, blockIdx.x, lane, WEIGHTED) : TokenMeta{-1, -1, 0.0f};
-    for (int j = 0; j < ntok && !*s_abort; ++j) {
-      const int t = blockIdx.x + j * gridDim.x;
-      TokenMeta nxt = cur;
-      if (j + 1 < ntok) nxt = fetch_meta(p, t + gridDim.x, lane, WEIGHTED);  // in flight meanwhile
+    int t = draw(0);
+    TokenMeta cur = t >= 0 ? fetch_meta(p, t, lane, WEIGHTED) : TokenMeta{-1, -1, 0.0f};
+    bool ok = true;
+    for (int j = 1; ok && !*s_abort; ++j) {
+      if (t < 0) {  // the end: a unit with n = -1 tells the reducers
+        const int s = static_cast<int>(i % kCombineStages);
+        if (i >= kCombineStages)
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], (uint32_t)(i / kCombineStages - 1) & 1u));
+        if (ok && lane == 0) {
+          *reinterpret_cast<int *>(stages + (size_t)s * kStageBytes) = -1;
+          mbar_arrive(&full[s]);
+          loads_issued = i + 1;
+        }
+        break;
+      }
+      const int t_next = draw(j);
+      const TokenMeta nxt = t_next >= 0 ? fetch_meta(p, t_next, lane, WEIGHTED) : cur;  // in flight meanwhile
       int slot = cur.slot;
       if (WEIGHTED && !layout_agrees(p, cur.e, slot, -1, lane) && lane == 0)
         set_error(p.error_word, EP_ERRBIT_STALE_LAYOUT);
@@ -319,19 +339,17 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
         const int elems = min(kChunk, p.H - c * kChunk);
         unsigned char *stage = stages + (size_t)s * kStageBytes;
         if (i >= kCombineStages) {
-          const bool ok = __all_sync(0xffffffffu,
-                                     mbar_wait_bounded(&empty[s], (uint32_t)(i / kCombineStages - 1) & 1u));
-          if (!ok) {
-            if (lane == 0) {
-              *s_abort = 1;
-              set_error(p.error_word, EP_ERRBIT_TIMEOUT);
-            }
-            break;
-          }
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], (uint32_t)(i / kCombineStages - 1) & 1u));
+          if (!ok) break;
         }
+        int *hdr = reinterpret_cast<int *>(stage);
         float *hdr_coef = reinterpret_cast<float *>(stage + 16);
         if (slot >= 0) hdr_coef[pos] = coef;
-        if (lane == 0) *reinterpret_cast<int *>(stage) = nrows;
+        if (lane == 0) {
+          hdr[0] = nrows;
+          hdr[1] = t;
+          hdr[2] = t_next;
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)nrows * (uint32_t)elems * 2u);
         __syncwarp();
@@ -340,33 +358,59 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
                     p.y + (size_t)slot * p.H + (size_t)c * kChunk, (uint32_t)elems * 2u, &full[s]);
         if (lane == 0) loads_issued = i + 1;
       }
+      t = t_next;
       cur = nxt;
     }
+    if (!ok && lane == 0) {
+      *s_abort = 1;
+      set_error(p.error_word, EP_ERRBIT_TIMEOUT);
+    }
+    if (lane == 0) retire_tokens(p.tokens, drained);
   } else {
     const int rt = tid - kWarpSize;  // reducer thread
     long i = 0;
-    for (int j = 0; j < ntok && !*s_abort; ++j) {
-      const int t = blockIdx.x + j * gridDim.x;
-      bool ok = true;
+    int known = -1;  // the token of the next unit, when a header has named it
+    bool more = true;
+    while (more && !*s_abort) {
       for (int c = 0; c < nchunk; ++c, ++i) {
         const int s = static_cast<int>(i % kCombineStages);
         const int cols = min(kChunk, p.H - c * kChunk) / 8;
         const unsigned char *stage = stages + (size_t)s * kStageBytes;
         // a unit has at most one column per reducer thread: its bias loads
-        // are issued before the wait for the rows
-        const size_t bcol = (size_t)t * p.H + (size_t)c * kChunk + (size_t)rt * 8;
+        // are issued before the wait for the rows when the token is known
         const int4 z = make_int4(0, 0, 0, 0);
-        const int4 b0 = (rt < cols && p.bias0) ? ld_stream_v4(p.bias0 + bcol) : z;
-        const int4 b1 = (rt < cols && p.bias1) ? ld_stream_v4(p.bias1 + bcol) : z;
+        int4 b0 = z, b1 = z;
+        auto load_bias = [&](int tok) {
+          const size_t bcol = (size_t)tok * p.H + (size_t)c * kChunk + (size_t)rt * 8;
+          if (rt < cols && p.bias0) b0 = ld_stream_v4(p.bias0 + bcol);
+          if (rt < cols && p.bias1) b1 = ld_stream_v4(p.bias1 + bcol);
+        };
+        if (known >= 0) load_bias(known);
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (uint32_t)(i / kCombineStages) & 1u))) {
           if (lane == 0) {
             *s_abort = 1;
             set_error(p.error_word, EP_ERRBIT_TIMEOUT);
           }
-          ok = false;
+          more = false;
           break;
         }
-        const int nrows = *reinterpret_cast<const int *>(stage);
+        const int *hdr = reinterpret_cast<const int *>(stage);
+        const int nrows = hdr[0];
+        if (nrows < 0) {  // the end
+          more = false;
+          break;
+        }
+        const int t = hdr[1];
+        const int t_next = hdr[2];
+        if (t < 0 || t >= p.T) {  // a hand-over that went wrong: stop, do not index with it
+          if (lane == 0) {
+            *s_abort = 1;
+            set_error(p.error_word, EP_ERRBIT_TIMEOUT);
+          }
+          more = false;
+          break;
+        }
+        if (known != t) load_bias(t);
         const float *hdr_coef = reinterpret_cast<const float *>(stage + 16);
         uint16_t *out = p.out + (size_t)t * p.H + (size_t)c * kChunk;
         static_assert(kChunk / 8 <= kReducers * kWarpSize, "one column per reducer thread");
@@ -388,8 +432,8 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
+        known = c + 1 < nchunk ? t : t_next;
       }
-      if (!ok) break;
     }
   }
 
@@ -466,6 +510,9 @@ ep_status_t launch_combine(const CombineArgs &a, cudaStream_t stream) {
   p.bias0 = a.bias0;
   p.bias1 = a.bias1;
   p.out = a.out;
+  p.tokens.ticket = a.work_counters;
+  p.tokens.done = a.work_counters != nullptr ? a.work_counters + 1 : nullptr;
+  p.tokens.T = a.num_tokens;
   const bool weighted = a.topk_weights != nullptr;
   if (kUseWsCombine && p.D <= kWsMaxRanks)
     return weighted ? launch_ws<true>(p, *di, stream) : launch_ws<false>(p, *di, stream);

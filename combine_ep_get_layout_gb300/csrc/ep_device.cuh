@@ -176,6 +176,22 @@ __device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
   return d;
 }
 
+// Hardware reciprocal approximation (PTX rcp.approx.f32, at most 1 ulp off
+// over the normal range; subnormal inputs are not flushed).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// (a * c, b * c), rounded to nearest even, as one packed f32x2 multiply.
+__device__ __forceinline__ void mul2_rn(float a, float b, float c, float &ac, float &bc) {
+  asm("{\n\t.reg .b64 t, k, u;\n\tmov.b64 t, {%2, %3};\n\tmov.b64 k, {%4, %4};\n\t"
+      "mul.rn.f32x2 u, t, k;\n\tmov.b64 {%0, %1}, u;\n\t}"
+      : "=f"(ac), "=f"(bc)
+      : "f"(a), "f"(b), "f"(c));
+}
+
 // ------------------------------------------------------------- grid barrier
 // For cooperative launches (all blocks co-resident).  The two words live in
 // caller-zeroed global memory; the last block out resets them, so the next
@@ -219,6 +235,43 @@ __device__ __forceinline__ void grid_barrier_exit(GridBarrierWords *bar) {
       atomicExch(&bar->depart, 0u);
     }
   }
+}
+
+// ------------------------------------------------------------- token source
+// The order in which the blocks of a dispatch or combine grid take tokens:
+// a fixed stripe per block (token blockIdx.x + i * gridDim.x), or tickets
+// from a grid-wide counter (`ticket` given), so that a block that starts
+// late or draws heavy tokens takes fewer.  One thread per block draws.
+// `done` counts the blocks that will draw no more; the last of them puts
+// both words back to zero for the next grid that uses them.
+
+struct TokenSource {
+  uint32_t *ticket;  // nullptr: fixed stripes
+  uint32_t *done;
+  int T;
+};
+
+// The drawing thread's block takes no more tokens (idempotent).
+__device__ __forceinline__ void retire_tokens(const TokenSource &ts, bool &drained) {
+  if (drained) return;
+  drained = true;
+  if (ts.ticket != nullptr && atomicAdd(ts.done, 1u) == gridDim.x - 1u) {
+    atomicExch(ts.ticket, 0u);
+    atomicExch(ts.done, 0u);
+  }
+}
+
+// The block's i-th token, or -1 once the tokens are exhausted (from then
+// on without touching the counter).  With a counter every token is drawn,
+// the first too: a block that starts late (its SM still busy with the
+// previous kernel) then owns no token yet.  `drained`: the drawing thread's
+// state, false at the start.
+__device__ __forceinline__ int draw_token(const TokenSource &ts, int i, bool &drained) {
+  if (drained) return -1;
+  const int t = ts.ticket == nullptr ? (int)blockIdx.x + i * (int)gridDim.x : (int)atomicAdd(ts.ticket, 1u);
+  if (t < ts.T) return t;
+  retire_tokens(ts, drained);
+  return -1;
 }
 
 // ------------------------------------------------- programmatic dependent launch

@@ -18,6 +18,7 @@
 //     ids, gate weights) and, for fp8, the scales.
 // Each row of x is read from HBM once and written once per destination rank.
 #include <algorithm>
+#include <climits>
 #include <mutex>
 
 #include "ep_device.cuh"
@@ -59,15 +60,45 @@ struct DispatchParams {
   uint32_t stage_stride;   // row_in_bytes rounded up to 128
   uint32_t out_stride;     // fp8 output row, H rounded up to 128
   uint32_t scale_stride;   // fp8 scales of one row, groups*4 rounded up to 16
+  TokenSource tokens;      // the order in which blocks take tokens
 };
 
-__device__ __forceinline__ void issue_row_load(const DispatchParams &p, unsigned char *stages,
-                                               uint64_t *full, int i, uint64_t policy) {
-  const int t = blockIdx.x + i * gridDim.x;
-  const int s = i % p.stages;
+// Token ids travel from the loading thread to the other roles of a block
+// through a ring of kTokRing shared ints: the block's idx-th token (or -1,
+// the end) in entry idx % kTokRing.  A loader is at most stages + 3 tokens
+// ahead of the slowest reader.
+constexpr int kTokRing = 16;
+constexpr int kTokPending = INT_MIN;       // entry not written yet
+constexpr int kTokTimedOut = INT_MIN + 1;  // wait_token gave up
+
+// Draws the block's idx-th token, records it in s_tok and starts the load
+// of its row into stage idx % stages (mbarrier full[stage]).  Once the
+// tokens are exhausted it records -1 and completes the stage's phase with a
+// plain arrival instead, so every index has a phase.  One thread.
+__device__ __forceinline__ void issue_token(const DispatchParams &p, unsigned char *stages, uint64_t *full,
+                                            volatile int *s_tok, int idx, bool &drained, uint64_t policy) {
+  const int t = draw_token(p.tokens, idx, drained);
+  const int s = idx % p.stages;
+  s_tok[idx % kTokRing] = t;
+  if (t < 0) {
+    mbar_arrive(&full[s]);
+    return;
+  }
   mbar_arrive_expect_tx(&full[s], p.row_in_bytes);
-  bulk_load_hint(stages + (size_t)s * p.stage_stride, p.x + (size_t)t * p.H, p.row_in_bytes,
-                 &full[s], policy);
+  bulk_load_hint(stages + (size_t)s * p.stage_stride, p.x + (size_t)t * p.H, p.row_in_bytes, &full[s], policy);
+}
+
+// The token in a ring entry once the loading thread has written it
+// (bounded wait: kTokTimedOut after kWaitLimitNs).
+__device__ __forceinline__ int wait_token(volatile int *entry) {
+  int t = *entry;
+  if (t != kTokPending) return t;
+  const uint64_t t0 = global_timer_ns();
+  while ((t = *entry) == kTokPending) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) return kTokTimedOut;
+    __nanosleep(32);
+  }
+  return t;
 }
 
 // Warp-collective: the layout holds exactly the rows this routing needs
@@ -92,16 +123,16 @@ __device__ __forceinline__ void count_received(const DispatchParams &p, int64_t 
   if (valid && slot >= 0 && slot < p.cap) atomicAdd(p.stats + e, 1u);
 }
 
-// Whether top-k slot k (expert e) is marked in the received row of
-// destination j, and the local expert id written there: a rank row marks
-// every expert of its rank; an expanded row marks only its own slot (TileScale
-// PR #68, commit message on the expanded combine).
-__device__ __forceinline__ bool marks(const DispatchParams &p, int64_t e, int k, int j) {
-  if (e < 0 || e >= p.E) return false;
-  return p.expanded ? k == j : static_cast<int>(e) / p.epr == j;
+// The destination whose received row marks top-k slot k (expert e), or -1:
+// a rank row marks every expert of its rank; an expanded row marks only its
+// own slot (TileScale PR #68, commit message on the expanded combine).  The
+// local expert id written there is e minus the rank's first expert.
+__device__ __forceinline__ int marked_dest(const DispatchParams &p, int64_t e, int k) {
+  if (e < 0 || e >= p.E) return -1;
+  return p.expanded ? k : static_cast<int>(e) / p.epr;
 }
 __device__ __forceinline__ int local_expert(const DispatchParams &p, int64_t e) {
-  return static_cast<int>(e) - (static_cast<int>(e) / p.epr) * p.epr;
+  return static_cast<int>(e) % p.epr;
 }
 
 // Received metadata of token t, by threads [32, blockDim): source token,
@@ -134,7 +165,7 @@ __device__ __forceinline__ void write_metadata(const DispatchParams &p, int t,
       const int slot = slots[j];
       if (slot < 0 || slot >= p.cap) continue;
       const int64_t e = __ldg(p.topk_idx + (size_t)t * p.K + k);
-      const bool here = marks(p, e, k, j);
+      const bool here = marked_dest(p, e, k) == j;
       if (p.recv_topk_idx != nullptr) p.recv_topk_idx[(size_t)slot * p.K + k] = here ? local_expert(p, e) : -1;
       if (p.recv_topk_weights != nullptr)
         p.recv_topk_weights[(size_t)slot * p.K + k] = here ? __ldg(p.topk_weights + (size_t)t * p.K + k) : 0.0f;
@@ -151,25 +182,82 @@ __device__ __forceinline__ void write_metadata(const DispatchParams &p, int t,
   }
 }
 
-// The fp8 cast of one 128-element group held by a warp, four bf16 values per
-// lane (`raw`, in element order): amax over the group by shuffles,
-// scale = amax / 448 and code = e4m3(x / scale) with IEEE division, round to
-// nearest even, saturating at +-448.  An all-zero group has scale 0 and keeps
-// each zero's sign.  Returns the lane's four codes (element order, low byte
-// first); `scale` receives the group's scale in every lane.
-__device__ __forceinline__ uint32_t cast_group(uint2 raw, float &scale) {
-  const float v0 = bf16_lo(raw.x), v1 = bf16_hi(raw.x);
-  const float v2 = bf16_lo(raw.y), v3 = bf16_hi(raw.y);
-  float a = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+// The fp8 cast of two 128-element groups held by a warp, one per half-warp,
+// eight bf16 values per lane (`raw`, in element order): amax over the group
+// by shuffles inside the half-warp, scale = amax / 448 and
+// code = e4m3(x / scale) with x / scale the correctly rounded fp32 quotient,
+// converted round to nearest even, saturating at +-448.  An all-zero group
+// has scale 0 and keeps each zero's sign.  Returns the lane's eight codes
+// (element order, low byte first); `scale` receives the group's scale in
+// every lane of the half-warp.
+//
+// The quotient is not divided out per element.  Ziv's rounding test: with
+// r = rcp_approx(scale), q = x * r lies within 2^-21 (relative) of x / scale,
+// and so does the correctly rounded quotient; q * (1 -+ 2^-19) bracket both.
+// The conversion is monotonic, so when the two ends of the bracket give the
+// same code, that is the code of the correctly rounded quotient.  Only a
+// lane with a quotient within about 2^-19 of a rounding boundary (and a
+// group whose scale is too small for r to be finite) divides.
+constexpr float kBracketBelow = 1.0f - 0x1p-19f;
+constexpr float kBracketAbove = 1.0f + 0x1p-19f;
+constexpr bool kCastPackedMul = true;  // f32x2 multiplies for the quotients and brackets
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  return pack_e4m3x2(a, b) | (pack_e4m3x2(c, d) << 16);
+}
+
+__device__ __forceinline__ void mul_pair(float a, float b, float c, float &ac, float &bc) {
+  if constexpr (kCastPackedMul) {
+    mul2_rn(a, b, c, ac, bc);
+  } else {
+    ac = a * c;
+    bc = b * c;
+  }
+}
+
+__device__ __forceinline__ uint2 cast_pair(uint4 raw, float &scale) {
+  float v[8] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y),
+                bf16_lo(raw.z), bf16_hi(raw.z), bf16_lo(raw.w), bf16_hi(raw.w)};
+  float a = fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
+                  fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+  for (int off = 8; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
   scale = __fdiv_rn(a, 448.0f);
-  const bool nz = a > 0.0f;
-  const float u0 = nz ? __fdiv_rn(v0, scale) : v0;
-  const float u1 = nz ? __fdiv_rn(v1, scale) : v1;
-  const float u2 = nz ? __fdiv_rn(v2, scale) : v2;
-  const float u3 = nz ? __fdiv_rn(v3, scale) : v3;
-  return pack_e4m3x2(u0, u1) | (pack_e4m3x2(u2, u3) << 16);
+  if (!(a > 0.0f)) return make_uint2(e4m3x4(v[0], v[1], v[2], v[3]), e4m3x4(v[4], v[5], v[6], v[7]));
+  if (scale >= 0x1p-125f) {  // 1 / scale is finite
+    const float r = rcp_approx(scale);
+    float q[8], lo[8], hi[8];
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      mul_pair(v[i], v[i + 1], r, q[i], q[i + 1]);
+      mul_pair(q[i], q[i + 1], kBracketBelow, lo[i], lo[i + 1]);
+      mul_pair(q[i], q[i + 1], kBracketAbove, hi[i], hi[i + 1]);
+    }
+    const uint2 cl = make_uint2(e4m3x4(lo[0], lo[1], lo[2], lo[3]), e4m3x4(lo[4], lo[5], lo[6], lo[7]));
+    const uint2 ch = make_uint2(e4m3x4(hi[0], hi[1], hi[2], hi[3]), e4m3x4(hi[4], hi[5], hi[6], hi[7]));
+    if (cl.x == ch.x && cl.y == ch.y) return cl;
+  }
+  float u[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) u[i] = __fdiv_rn(v[i], scale);
+  return make_uint2(e4m3x4(u[0], u[1], u[2], u[3]), e4m3x4(u[4], u[5], u[6], u[7]));
+}
+
+// Casts groups [g0, g0 + 2) of a staged bf16 row (`stage`, 256 bytes per
+// group) into `orow` (128 codes per group) and `oscale`; a group index at or
+// past `groups` is skipped.  Warp-collective.
+__device__ __forceinline__ void cast_two_groups(const unsigned char *stage, unsigned char *orow, float *oscale,
+                                                int g0, int groups, int lane) {
+  const int g = g0 + (lane >> 4);
+  const bool live = g < groups;
+  const uint4 raw = live ? *reinterpret_cast<const uint4 *>(stage + (size_t)g0 * 256 + lane * 16)
+                         : make_uint4(0u, 0u, 0u, 0u);
+  float scale;
+  const uint2 codes = cast_pair(raw, scale);
+  if (live) {
+    *reinterpret_cast<uint2 *>(orow + (size_t)g0 * 128 + lane * 8) = codes;
+    if ((lane & 15) == 0) oscale[g] = scale;
+  }
 }
 
 template <bool FP8>
@@ -178,6 +266,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(Dispatc
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);               // [kMaxStages]
   int *s_abort = reinterpret_cast<int *>(smem + 64);
   int32_t *s_slot = reinterpret_cast<int32_t *>(smem + 128);         // [2][EP_MAX_RANKS]
+  volatile int *s_tok = reinterpret_cast<volatile int *>(smem + 640);  // [kTokRing]
   unsigned char *stages = smem + kHeaderBytes;
   unsigned char *obuf = stages + (size_t)p.stages * p.stage_stride;  // fp8: [2][out_stride]
   float *sbuf = reinterpret_cast<float *>(obuf + 2 * (size_t)p.out_stride);  // fp8: [2][groups]
@@ -186,8 +275,8 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(Dispatc
   const int warp = tid / kWarpSize;
   const int lane = tid & (kWarpSize - 1);
   const int S = p.stages;
-  const int n = (p.T > (int)blockIdx.x) ? (p.T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 
+  if (tid < kTokRing) s_tok[tid] = kTokPending;
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
     *s_abort = 0;
@@ -197,13 +286,24 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(Dispatc
   griddep_wait();
   griddep_launch_dependents();
   const uint64_t policy = policy_evict_first();  // x is read exactly once
-  int loads_issued = 0;                           // meaningful in thread 0 only
+  bool drained = false;  // thread 0: no more tokens to draw
+  int issued = 0;        // thread 0: token indices drawn (loads and the end)
   if (tid == 0)
-    for (; loads_issued < min(S, n); ++loads_issued) issue_row_load(p, stages, full, loads_issued, policy);
+    for (; issued < S && !drained; ++issued) issue_token(p, stages, full, s_tok, issued, drained, policy);
+  __syncthreads();
 
   int i = 0;
-  for (; i < n; ++i) {
-    const int t = blockIdx.x + i * gridDim.x;
+  for (;; ++i) {
+    // Thread 0 may have drawn token i during the previous iteration, after
+    // that iteration's last barrier (bf16 with two stages): this barrier
+    // makes its ring entry visible.
+    if (i > 0) __syncthreads();
+    const int t = s_tok[i % kTokRing];
+    if (t < 0) break;  // the end (or an entry never written)
+    if (t >= p.T) {    // a hand-over that went wrong: stop, do not index with it
+      if (tid == 0) set_error(p.error_word, EP_ERRBIT_TIMEOUT);
+      break;
+    }
     const int s = i % S;
     const uint32_t parity = (uint32_t)(i / S) & 1u;
     const int b = i & 1;
@@ -225,17 +325,13 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(Dispatc
       }
       unsigned char *orow = obuf + (size_t)b * p.out_stride;
       float *srow = sbuf + (size_t)b * (p.scale_stride / 4);
-      for (int g = warp; g < p.groups; g += kDispatchWarps) {
-        float scale;
-        const uint2 raw = *reinterpret_cast<const uint2 *>(stage + (size_t)g * 256 + lane * 8);
-        *reinterpret_cast<uint32_t *>(orow + (size_t)g * 128 + lane * 4) = cast_group(raw, scale);
-        if (lane == 0) srow[g] = scale;
-      }
+      for (int g0 = 2 * warp; g0 < p.groups; g0 += 2 * kDispatchWarps)
+        cast_two_groups(stage, orow, srow, g0, p.groups, lane);
       fence_proxy_async_smem();
       __syncthreads();
       if (*s_abort) break;
       if (warp == 0) {
-        if (lane == 0 && i + S < n) issue_row_load(p, stages, full, loads_issued++, policy);
+        if (lane == 0 && !drained) issue_token(p, stages, full, s_tok, issued++, drained, policy);
         for (int j = lane; j < p.D; j += kWarpSize) {
           const int slot = slots[j];
           if (slot < 0) continue;
@@ -271,7 +367,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(Dispatc
           // the stores of token i-1 have read their stage: reload it
           bulk_wait_read<1>();
           __syncwarp();
-          if (lane == 0 && i >= 1 && i - 1 + S < n) issue_row_load(p, stages, full, loads_issued++, policy);
+          if (lane == 0 && i >= 1 && !drained) issue_token(p, stages, full, s_tok, issued++, drained, policy);
         }
       } else {
         write_metadata<false>(p, t, slots, nullptr);
@@ -281,10 +377,11 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(Dispatc
 
   // Drain: stores must finish reading shared memory before the CTA exits;
   // after an abort, loads still in flight are waited for (bounded).
+  if (tid == 0) retire_tokens(p.tokens, drained);
   if (warp == 0) bulk_wait<0>();
   __syncthreads();
   if (*s_abort && tid == 0) {
-    for (int m = i; m < loads_issued; ++m) (void)mbar_wait_bounded(&full[m % S], (uint32_t)(m / S) & 1u);
+    for (int m = i; m < issued; ++m) (void)mbar_wait_bounded(&full[m % S], (uint32_t)(m / S) & 1u);
   }
 }
 
@@ -307,7 +404,26 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(Dispatc
 
 constexpr int kWsCasters = 8;
 constexpr int kWsThreads = (2 + kWsCasters) * kWarpSize;
-constexpr int kWsOut = 2;
+constexpr int kWsOut = 3;
+// The storer releases an output buffer one token late (once the next
+// token's stores are issued), so waiting for the stores to read a buffer
+// overlaps the next token's metadata instead of preceding it.
+constexpr bool kWsLateRelease = true;
+
+// Storer, after committing token i's stores: hand an output buffer back to
+// the casters once the bulk stores have read it -- token i's buffer, or with
+// late release token i-1's (the stores of token i may still be reading).
+__device__ __forceinline__ void release_out(uint64_t *empty_out, int i, int lane) {
+  if constexpr (kWsLateRelease) {
+    bulk_wait_read<1>();
+    __syncwarp();
+    if (lane == 0 && i > 0) mbar_arrive(&empty_out[(i - 1) % kWsOut]);
+  } else {
+    bulk_wait_read<0>();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_out[i % kWsOut]);
+  }
+}
 
 __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -318,6 +434,7 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
   uint64_t *empty_out = full_out + kWsOut;                  // [kWsOut]
   volatile int *s_abort = reinterpret_cast<volatile int *>(smem + 256);
   int32_t *s_slot = reinterpret_cast<int32_t *>(smem + 512);  // [EP_MAX_RANKS], storer only
+  volatile int *s_tok = reinterpret_cast<volatile int *>(smem + 768);  // [kTokRing]
   unsigned char *in = smem + kHeaderBytes;
   unsigned char *out = in + (size_t)S * p.stage_stride;
   float *osc = reinterpret_cast<float *>(out + (size_t)kWsOut * p.out_stride);
@@ -325,8 +442,8 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
   const int tid = threadIdx.x;
   const int warp = tid / kWarpSize;
   const int lane = tid & (kWarpSize - 1);
-  const int n = (p.T > (int)blockIdx.x) ? (p.T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 
+  if (tid < kTokRing) s_tok[tid] = kTokPending;
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_in[s], 1);
@@ -349,34 +466,50 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
   griddep_wait();
   griddep_launch_dependents();
 
-  int loads_issued = 0;  // loader lane 0 only
+  int issued = 0;        // loader lane 0: token indices drawn (loads and the end)
+  bool drained = false;  // loader lane 0: no more tokens to draw
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t policy = policy_evict_first();
-      for (int i = 0; i < n && !*s_abort; ++i) {
+      for (int i = 0; !drained && !*s_abort; ++i) {
         const int s = i % S;
         if (i >= S && !mbar_wait_bounded(&empty_in[s], (uint32_t)(i / S - 1) & 1u)) {
           *s_abort = 1;
           set_error(p.error_word, EP_ERRBIT_TIMEOUT);
           break;
         }
-        const int t = blockIdx.x + i * gridDim.x;
-        mbar_arrive_expect_tx(&full_in[s], p.row_in_bytes);
-        bulk_load_hint(in + (size_t)s * p.stage_stride, p.x + (size_t)t * p.H, p.row_in_bytes, &full_in[s],
-                       policy);
-        loads_issued = i + 1;
+        issue_token(p, in, full_in, s_tok, i, drained, policy);
+        issued = i + 1;
       }
+      retire_tokens(p.tokens, drained);
     }
   } else if (warp == 1) {
     const bool scale_bulk = p.scale_stride == (uint32_t)p.groups * 4u &&
                             (reinterpret_cast<uintptr_t>(p.recv_x_scales) & 15u) == 0;
-    for (int i = 0; i < n && !*s_abort; ++i) {
-      const int t = blockIdx.x + i * gridDim.x;
+    for (int i = 0; !*s_abort; ++i) {
+      const int t = wait_token(&s_tok[i % kTokRing]);
+      if (t == kTokTimedOut) {
+        if (lane == 0) {
+          *s_abort = 1;
+          set_error(p.error_word, EP_ERRBIT_TIMEOUT);
+        }
+        break;
+      }
+      if (t < 0) break;
+      if (t >= p.T) {  // a hand-over that went wrong: stop, do not index with it
+        if (lane == 0) {
+          *s_abort = 1;
+          set_error(p.error_word, EP_ERRBIT_TIMEOUT);
+        }
+        break;
+      }
       const int o = i % kWsOut;
       const int32_t *srow = p.token_slot + (size_t)t * p.D;
       int slot_lo = lane < p.D ? __ldg(srow + lane) : -1;
       int slot_hi = lane + kWarpSize < p.D ? __ldg(srow + lane + kWarpSize) : -1;
       const int64_t e = lane < p.K ? __ldg(p.topk_idx + (size_t)t * p.K + lane) : -1;
+      const float w = (lane < p.K && p.recv_topk_weights != nullptr)
+                          ? __ldg(p.topk_weights + (size_t)t * p.K + lane) : 0.0f;
       if (!layout_agrees(p, e, slot_lo, slot_hi, lane) && lane == 0)
         set_error(p.error_word, EP_ERRBIT_STALE_LAYOUT);
       if (slot_lo >= p.cap) {
@@ -388,17 +521,16 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
         slot_hi = -1;
       }
       if (p.stats != nullptr) count_received(p, e, slot_lo, slot_hi, lane);
-      const float w = (lane < p.K && p.recv_topk_weights != nullptr)
-                          ? __ldg(p.topk_weights + (size_t)t * p.K + lane) : 0.0f;
+      const int dest = marked_dest(p, e, lane);
+      const int local = dest >= 0 ? local_expert(p, e) : -1;
       // received metadata: needs no shared memory, runs ahead of the cast
       for (int r = 0; r < p.D; ++r) {
         const int slot = __shfl_sync(0xffffffffu, r < kWarpSize ? slot_lo : slot_hi, r & (kWarpSize - 1));
         if (slot < 0) continue;
         if (lane == 0 && p.recv_src_idx != nullptr) p.recv_src_idx[slot] = t;
         if (lane < p.K) {
-          const bool here = marks(p, e, lane, r);
-          if (p.recv_topk_idx != nullptr)
-            p.recv_topk_idx[(size_t)slot * p.K + lane] = here ? local_expert(p, e) : -1;
+          const bool here = dest == r;
+          if (p.recv_topk_idx != nullptr) p.recv_topk_idx[(size_t)slot * p.K + lane] = here ? local : -1;
           if (p.recv_topk_weights != nullptr) p.recv_topk_weights[(size_t)slot * p.K + lane] = here ? w : 0.0f;
         }
       }
@@ -410,6 +542,8 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
         }
         break;
       }
+      __syncwarp();
+      if (lane == 0) s_tok[i % kTokRing] = kTokPending;  // every caster has read it
       const unsigned char *orow = out + (size_t)o * p.out_stride;
       const float *oscale = osc + (size_t)o * (p.scale_stride / 4);
       if (p.packed) {  // codes, scales and padding go out as one row
@@ -420,9 +554,7 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
           bulk_store(static_cast<unsigned char *>(p.recv_x) + (size_t)slot_hi * p.row_out_bytes, orow,
                      p.row_out_bytes);
         bulk_commit();
-        bulk_wait_read<0>();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_out[o]);
+        release_out(empty_out, i, lane);
         continue;
       }
       if (slot_lo >= 0) {
@@ -446,18 +578,25 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
           if (slot >= 0) p.recv_x_scales[(size_t)slot * p.groups + g] = oscale[g];
         }
       }
-      bulk_wait_read<0>();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_out[o]);
+      release_out(empty_out, i, lane);
     }
     bulk_wait<0>();
   } else {
     const int cw = warp - 2;
-    for (int i = 0; i < n && !*s_abort; ++i) {
+    for (int i = 0; !*s_abort; ++i) {
       const int s = i % S;
       const int o = i % kWsOut;
       bool ok = mbar_wait_bounded(&full_in[s], (uint32_t)(i / S) & 1u);
-      if (ok && i >= kWsOut) ok = mbar_wait_bounded(&empty_out[o], (uint32_t)(i / kWsOut - 1) & 1u);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) {
+          *s_abort = 1;
+          set_error(p.error_word, EP_ERRBIT_TIMEOUT);
+        }
+        break;
+      }
+      const int tc = s_tok[i % kTokRing];
+      if (tc < 0 || tc >= p.T) break;  // the end (the storer flags a bad entry)
+      if (i >= kWsOut) ok = mbar_wait_bounded(&empty_out[o], (uint32_t)(i / kWsOut - 1) & 1u);
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) {
           *s_abort = 1;
@@ -468,12 +607,8 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
       const unsigned char *stage = in + (size_t)s * p.stage_stride;
       unsigned char *orow = out + (size_t)o * p.out_stride;
       float *oscale = p.packed ? reinterpret_cast<float *>(orow + p.H) : osc + (size_t)o * (p.scale_stride / 4);
-      for (int g = cw; g < p.groups; g += kWsCasters) {
-        float scale;
-        const uint2 raw = *reinterpret_cast<const uint2 *>(stage + (size_t)g * 256 + lane * 8);
-        *reinterpret_cast<uint32_t *>(orow + (size_t)g * 128 + lane * 4) = cast_group(raw, scale);
-        if (lane == 0) oscale[g] = scale;
-      }
+      for (int g0 = 2 * cw; g0 < p.groups; g0 += 2 * kWsCasters)
+        cast_two_groups(stage, orow, oscale, g0, p.groups, lane);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -488,8 +623,7 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
   // (the last S issued) can still be in flight.
   __syncthreads();
   if (*s_abort && tid == 0) {
-    for (int m = max(0, loads_issued - S); m < loads_issued; ++m)
-      (void)mbar_wait_bounded(&full_in[m % S], (uint32_t)(m / S) & 1u);
+    for (int m = max(0, issued - S); m < issued; ++m) (void)mbar_wait_bounded(&full_in[m % S], (uint32_t)(m / S) & 1u);
   }
 }
 
@@ -639,6 +773,9 @@ ep_status_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream) {
   p.stage_stride = (p.row_in_bytes + 127u) / 128u * 128u;
   p.out_stride = a.fp8 ? (p.row_out_bytes + 127u) / 128u * 128u : 0u;
   p.scale_stride = (a.fp8 && !p.packed) ? ((uint32_t)p.groups * 4u + 15u) / 16u * 16u : 0u;
+  p.tokens.ticket = a.work_counters;
+  p.tokens.done = a.work_counters != nullptr ? a.work_counters + 1 : nullptr;
+  p.tokens.T = a.num_tokens;
   ep_status_t st = EP_OK;
   if (a.num_tokens > 0) {
     // packed rows are only built by the warp-specialised kernel

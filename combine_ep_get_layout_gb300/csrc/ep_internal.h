@@ -67,6 +67,7 @@ struct DispatchArgs {
   bool zero_padding;                   // expanded: write the padding rows
   bool fp8;
   int packed_row_bytes;  // > 0: packed fp8 rows of this many bytes
+  uint32_t *work_counters;  // 2 words (ticket, done) or null: fixed token stripes
   void *recv_x;
   float *recv_x_scales;
   int32_t *recv_src_idx;
@@ -88,6 +89,7 @@ struct CombineArgs {
   const float *topk_weights;
   const uint16_t *bias0, *bias1;  // [T*H] or null
   uint16_t *out;
+  uint32_t *work_counters;  // 2 words (ticket, done) or null: fixed token stripes
 };
 ep_status_t launch_combine(const CombineArgs &a, cudaStream_t stream);
 

@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutParams p) 
     // Cleared before the barrier; every block adds into them after it.
     for (int i = tid; i < E; i += kLayoutThreads) p.out.num_tokens_per_expert[i] = 0;
     if (tid == 0) *p.out.error_word = 0u;
+    if (tid < EP_WORK_COUNTER_WORDS && p.out.work_counters != nullptr) p.out.work_counters[tid] = 0u;
   }
   __syncthreads();
 

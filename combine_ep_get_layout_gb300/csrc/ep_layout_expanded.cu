@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(kXThreads) layout_expanded_kernel(XLayoutParam
   griddep_wait();
   griddep_launch_dependents();
   if (b == 0 && tid == 0) *p.out.error_word = 0u;
+  if (b == 0 && tid < EP_WORK_COUNTER_WORDS && p.out.work_counters != nullptr) p.out.work_counters[tid] = 0u;
   __syncthreads();
 
   const int begin = min(b * p.tokens_per_block, p.T);

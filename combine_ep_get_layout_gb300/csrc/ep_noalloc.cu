@@ -71,7 +71,8 @@ extern "C" ep_status_t ep_get_layout_noalloc(const int64_t *topk_idx, int num_to
     return fail(EP_ERR_INVALID_ARG, "%s: layout or one of its arrays is NULL", fn);
   if (!aligned(layout->num_tokens_per_expert, 4) || !aligned(layout->num_tokens_per_rank, 4) ||
       !aligned(layout->rank_prefix, 4) || !aligned(layout->error_word, 4) ||
-      !aligned(layout->is_token_in_rank, 16) || !aligned(layout->token_slot, 16))
+      !aligned(layout->is_token_in_rank, 16) || !aligned(layout->token_slot, 16) ||
+      !aligned(layout->work_counters, 16))
     return fail(EP_ERR_INVALID_ARG, "%s: a layout array is misaligned", fn);
   const size_t need = layout_workspace_bytes(num_tokens, num_experts, num_ranks);
   if (need > EP_NOALLOC_SCRATCH_BYTES)

@@ -64,7 +64,8 @@ typedef enum {
 /* Bits of the device error word (ep_layout_t.error_word). */
 #define EP_ERRBIT_BAD_INDEX 0x1u  /* a topk_idx entry outside [-1, E)        */
 #define EP_ERRBIT_CAPACITY 0x2u   /* a row's slot >= recv_capacity: skipped  */
-#define EP_ERRBIT_TIMEOUT 0x4u    /* a bounded device wait gave up           */
+#define EP_ERRBIT_TIMEOUT 0x4u    /* a bounded device wait gave up (or a hand-
+                                     over between a kernel's roles failed)   */
 #define EP_ERRBIT_STALE_LAYOUT 0x8u /* routing and layout disagree on a token's
                                        set of ranks (a layout of another routing) */
 #define EP_ERRBIT_DUP_EXPERT 0x10u  /* expanded layout: a token names an expert
@@ -96,9 +97,21 @@ typedef enum {
  *   error_word            [1]   uint32: EP_ERRBIT_* flags.  ep_get_layout
  *                               clears it; ep_dispatch and ep_combine given
  *                               this layout OR their bits into it.
+ *   work_counters  [EP_WORK_COUNTER_WORDS] uint32, 16-byte aligned, or
+ *                               NULL.  Given, ep_dispatch and ep_combine hand
+ *                               tokens to their thread blocks from a
+ *                               grid-wide counter in these words (a block
+ *                               that starts late, or draws tokens with many
+ *                               destinations, takes fewer), instead of a
+ *                               fixed stripe of tokens per block.  The words
+ *                               must be zero when a call starts: ep_get_layout
+ *                               zeroes them and every call leaves them zero.
+ *                               Calls sharing them must be ordered (the same
+ *                               stream, or events).  No effect on any result.
  * The layout is the single-GPU counterpart of the count matrix and
  * send_base[d] + slot of TileScale PR #68 (README section "Design").
  */
+#define EP_WORK_COUNTER_WORDS 4
 typedef struct {
     int32_t *num_tokens_per_expert;
     int32_t *num_tokens_per_rank;
@@ -106,6 +119,7 @@ typedef struct {
     uint8_t *is_token_in_rank;
     int32_t *token_slot;
     uint32_t *error_word;
+    uint32_t *work_counters;
 } ep_layout_t;
 
 /*
@@ -344,12 +358,15 @@ ep_status_t ep_combine_ex(const ep_combine_args_t *args, ep_stream_t stream);
  *                             expert already named by t).  Inside a block
  *                             rows are in ascending (token, k) order.
  *   error_word          [1]   uint32: EP_ERRBIT_* (cleared by the layout).
+ *   work_counters       [EP_WORK_COUNTER_WORDS] uint32 or NULL: as in
+ *                             ep_layout_t (zeroed by ep_get_layout_expanded).
  */
 typedef struct {
     int32_t *num_rows_per_expert;
     int32_t *expert_offset;
     int32_t *token_slot;
     uint32_t *error_word;
+    uint32_t *work_counters;
 } ep_expanded_layout_t;
 
 /* Workspace bytes of ep_get_layout_expanded (zero-filled once at
@@ -436,7 +453,7 @@ const char *ep_status_str(ep_status_t status);
 const char *ep_last_error(void);
 
 /* ABI version of this header: bumped on any incompatible change. */
-#define EP_ABI_VERSION 1
+#define EP_ABI_VERSION 2
 int ep_abi_version(void);
 
 #ifdef __cplusplus

@@ -36,12 +36,12 @@ def layout_np(lay: ep.Layout) -> dict:
 
 
 def run_gpu_path(x_bits, topk_idx, topk_weights, E, R, fp8, cap, y_bits=None,
-                 weighted=True, stream=None):
+                 weighted=True, stream=None, work_counters=True):
     """Layout, dispatch and combine on cuda:0 through the binding."""
     x = to_dev_bf16(x_bits)
     idx = torch.from_numpy(np.ascontiguousarray(topk_idx)).to(dev())
     w = torch.from_numpy(np.ascontiguousarray(topk_weights)).to(dev())
-    lay = ep.ep_get_layout(idx, E, R, stream=stream)
+    lay = ep.ep_get_layout(idx, E, R, stream=stream, work_counters=work_counters)
     d = ep.ep_dispatch(x, idx, w, lay, dtype="fp8" if fp8 else "bf16", recv_capacity=cap,
                        stream=stream)
     y = d.recv_x if y_bits is None else to_dev_bf16(y_bits)
@@ -56,6 +56,7 @@ def run_gpu_path(x_bits, topk_idx, topk_weights, E, R, fp8, cap, y_bits=None,
         "recv_topk_idx": bits(d.recv_topk_idx),
         "recv_topk_weights": bits(d.recv_topk_weights),
         "combined": bits(out),
+        "work_counters": None if lay.work_counters is None else bits(lay.work_counters),
     }
 
 

@@ -151,7 +151,9 @@ def test_combine_rejects(lib, kw, needle):
 def test_status_strings(lib):
     assert [lib.ep_status_str(i).decode() for i in range(4)] == [
         "EP_OK", "EP_ERR_INVALID_ARG", "EP_ERR_UNSUPPORTED", "EP_ERR_CUDA"]
-    assert lib.ep_abi_version() == 1
+    from combine_ep_get_layout_gb300 import _native as N
+    text = "".join(open(h).read() for h in HEADERS)
+    assert lib.ep_abi_version() == N.ABI_VERSION == int(re.search(r"EP_ABI_VERSION (\d+)", text).group(1))
 
 
 def test_packed_row_bytes_matches_oracle(lib):
@@ -294,3 +296,30 @@ def test_combine_expanded_rejects(lib, kw, needle):
     name, msg = _status(lib, lib.ep_combine_expanded(C.byref(args), None))
     assert name == "EP_ERR_INVALID_ARG", (name, msg)
     assert needle in msg
+
+
+def test_work_counters_must_be_16_byte_aligned(lib):
+    from combine_ep_get_layout_gb300 import _native as N
+    lay = _layout()
+    lay.work_counters = 0x30004
+    s = lib.ep_get_layout(FAKE, 100, 4, 16, 4, C.byref(lay), FAKE, 1 << 20, None)
+    name, msg = _status(lib, s)
+    assert name == "EP_ERR_INVALID_ARG" and "work_counters" in msg
+    s = lib.ep_get_layout_noalloc(FAKE, 100, 4, 16, 4, C.byref(lay), None)
+    assert _status(lib, s)[0] == "EP_ERR_INVALID_ARG"
+    a, _keep = _dargs()
+    a.layout.contents.work_counters = 0x30008
+    name, msg = _status(lib, lib.ep_dispatch_ex(C.byref(a), None))
+    assert name == "EP_ERR_INVALID_ARG" and "work_counters" in msg
+    cargs = N.ep_combine_args_t(0x20000, 400, 256, C.pointer(lay), 100, 4, 0x20000, 0x20000, 4, 16,
+                                None, None, 0x20000)
+    name, msg = _status(lib, lib.ep_combine_ex(C.byref(cargs), None))
+    assert name == "EP_ERR_INVALID_ARG" and "work_counters" in msg
+    xl = _xlayout()
+    xl.work_counters = 0x30002
+    s = lib.ep_get_layout_expanded(FAKE, 100, 4, 16, 8, C.byref(xl), FAKE, 1 << 20, None)
+    name, msg = _status(lib, s)
+    assert name == "EP_ERR_INVALID_ARG" and "work_counters" in msg
+    xd, _keep2 = _xdargs(lay=xl)
+    name, msg = _status(lib, lib.ep_dispatch_expanded(C.byref(xd), None))
+    assert name == "EP_ERR_INVALID_ARG" and "work_counters" in msg

@@ -30,7 +30,7 @@ def _cuda():
 import gpu_util as U  # noqa: E402
 
 
-def _full_case(cfg, weighted=True, cap=None, y_seed=1):
+def _full_case(cfg, weighted=True, cap=None, y_seed=1, work_counters=True):
     inp = W.make(cfg)
     E, R, fp8 = cfg.num_experts, cfg.num_ranks, cfg.fp8
     cap = W.recv_capacity(cfg) if cap is None else cap
@@ -38,7 +38,7 @@ def _full_case(cfg, weighted=True, cap=None, y_seed=1):
     N = int(lay_o["rank_prefix"][R])
     y = W.expert_output(cap, cfg.hidden, seed=y_seed) if fp8 else None
     g = U.run_gpu_path(inp["x"], inp["topk_idx"], inp["topk_weights"], E, R, fp8, cap,
-                       y_bits=y, weighted=weighted)
+                       y_bits=y, weighted=weighted, work_counters=work_counters)
     d_o = oracle.dispatch(inp["x"], inp["topk_idx"], inp["topk_weights"], E, R,
                           lay_o["token_slot"], fp8, cap)
     # bf16: a round trip combines the dispatched rows themselves
@@ -295,3 +295,19 @@ def test_cached_layout_and_stale_guard(dtype):
     o = oracle.dispatch(inp["x"], moved_np, inp["topk_weights"], E, R, U.bits(lay.token_slot),
                         False, N)
     assert o["error"] & oracle.STALE
+
+
+@pytest.mark.parametrize("name", ["bf16_4096x4096_top6_64e", "fp8_8192x7168_top8_256e"])
+@pytest.mark.parametrize("work_counters", [True, False], ids=["counter", "stripes"])
+def test_token_order_modes(name, work_counters):
+    """Blocks drawing tokens from the layout's work counters, or taking fixed
+    stripes (no counters): the same results; the counters are left zero."""
+    cfg = W.CONFIGS[name]
+    g, lay_o, d_o, c_o, N = _full_case(cfg, weighted=True, work_counters=work_counters)
+    U.assert_layout_equal(g["layout"], lay_o)
+    U.assert_dispatch_equal(g, d_o, N, cfg.fp8)
+    assert np.array_equal(g["combined"], c_o)
+    if work_counters:
+        assert g["work_counters"].tolist() == [0, 0, 0, 0]
+    else:
+        assert g["work_counters"] is None
