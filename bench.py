@@ -388,6 +388,10 @@ def run_ours(args, rank, world, local):
     # (3) end to end through the public binding, host buffers, copies included.
     e2e = None if args.no_e2e else run_e2e(args, cfg, inp, y_np, cap, dev, world)
 
+    # (4) the next rows (cached layout, packed rows, expanded path, bias and
+    # stats) on the same workload: secondary numbers, after the timed region.
+    next_rows = None if (args.no_next_rows or not cfg.fp8) else run_next_rows(cfg, x, idx, w, y, cap, lay, peak)
+
     if rank != 0:
         return 0
     line = {
@@ -399,10 +403,107 @@ def run_ours(args, rank, world, local):
         "kernels": kernels, "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
         "clocks": clocks.summary(), "wall_s_timed_region": round(t_wall, 4),
     }
+    if next_rows is not None:
+        line["next_rows"] = next_rows
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, inp, y_np)
     print(json.dumps(line), flush=True)
     return 0
+
+
+def _time_calls(fns, reps, stream):
+    """Mean device time of each call in ``fns`` (an event between calls),
+    and of the whole sequence run back to back without events between
+    calls (so programmatic dependent launch still overlaps them)."""
+    for _ in range(3):
+        for f in fns:
+            f()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)] for _ in range(reps)]
+    for e in evs:
+        for j, f in enumerate(fns):
+            e[j].record(stream)
+            f()
+        e[-1].record(stream)
+    torch.cuda.synchronize()
+    each = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) * 1e3 for j in range(len(fns))]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        for f in fns:
+            f()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return each, e0.elapsed_time(e1) * 1e3 / reps
+
+
+def run_next_rows(cfg, x, idx, w, y, cap, lay, peak, reps=200):
+    """The ranked next rows on the same workload, through the binding:
+    a cached layout (dispatch and combine only), packed fp8 rows, the
+    expanded (per-expert) path, cumulative receive stats with combine
+    biases.  Device times, CUDA events on the launching stream."""
+    import combine_ep_get_layout_gb300 as ep
+    T, H, K, E, R = cfg.num_tokens, cfg.hidden, cfg.num_topk, cfg.num_experts, cfg.num_ranks
+    dev = x.device
+    stream = torch.cuda.current_stream(dev)
+    N = lay.num_recv()
+    G = H // 128
+    rnd = lambda v: round(v, 2)  # noqa: E731
+    frac = lambda b, us: round(b / (us * 1e-6) / 1e9 / peak, 4)  # noqa: E731
+    meta = T * K * 12 + T * R * 4
+    out = {}
+
+    # cached layout: the routing is unchanged, so the layout is not recomputed
+    d8 = ep.ep_dispatch(x, idx, w, lay, dtype="fp8", recv_capacity=cap)
+    o = ep.ep_combine(y, lay, idx, w)
+    (t_d, t_c), step = _time_calls(
+        [lambda: ep.ep_dispatch(x, idx, w, lay, dtype="fp8", recv_capacity=cap, out=d8),
+         lambda: ep.ep_combine(y, lay, idx, w, out=o)], reps, stream)
+    out["cached_layout"] = {"step_us": rnd(step), "dispatch_us": rnd(t_d), "combine_us": rnd(t_c)}
+
+    # packed fp8 rows: codes, scales and padding in one row
+    P = ep.ep_fp8_packed_row_bytes(H)
+    dp = ep.ep_dispatch(x, idx, w, lay, dtype="fp8_packed", recv_capacity=cap)
+    (t_p,), _ = _time_calls(
+        [lambda: ep.ep_dispatch(x, idx, w, lay, dtype="fp8_packed", recv_capacity=cap, out=dp)], reps, stream)
+    b_p = T * H * 2 + N * P + N * (4 + 8 * K) + meta
+    b_s = T * H * 2 + N * (H + 4 * G) + N * (4 + 8 * K) + meta
+    out["fp8_packed"] = {"row_bytes": P, "dispatch_us": rnd(t_p), "algorithmic_bytes": b_p,
+                         "frac": frac(b_p, t_p), "separate_scales_dispatch_us": rnd(t_d),
+                         "separate_scales_frac": frac(b_s, t_d)}
+
+    # expanded: one row per (token, expert), blocks aligned to 128 rows
+    A = 128
+    xl = ep.ep_get_layout_expanded(idx, E, A)
+    M = xl.num_rows()
+    dx = ep.ep_dispatch_expanded(x, idx, w, xl, R, dtype="fp8", recv_capacity=M)
+    gen = torch.Generator(device=dev).manual_seed(1)
+    dx_y = torch.randn((M, H), device=dev, generator=gen).bfloat16()  # the experts' output rows
+    ox = ep.ep_combine_expanded(dx_y, xl, idx, w)
+    (t_xl, t_xd, t_xc), x_step = _time_calls(
+        [lambda: ep.ep_get_layout_expanded(idx, E, A, layout=xl),
+         lambda: ep.ep_dispatch_expanded(x, idx, w, xl, R, dtype="fp8", recv_capacity=M, out=dx),
+         lambda: ep.ep_combine_expanded(dx_y, xl, idx, w, out=ox)], reps, stream)
+    NK = int((idx >= 0).sum().item())
+    b_xd = T * H * 2 + M * (H + 4 * G) + M * (4 + 8 * K) + T * K * 16
+    b_xc = NK * H * 2 + T * H * 2 + T * K * 16
+    out["expanded"] = {"alignment": A, "rows": M, "selections": NK, "layout_us": rnd(t_xl),
+                       "dispatch_us": rnd(t_xd), "dispatch_frac": frac(b_xd, t_xd),
+                       "combine_us": rnd(t_xc), "combine_frac": frac(b_xc, t_xc), "step_us": rnd(x_step)}
+
+    # cumulative receive stats on the dispatch, two biases on the combine
+    stats = torch.zeros(E, dtype=torch.int32, device=dev)
+    b0 = torch.randn((T, H), device=dev).bfloat16()
+    b1 = torch.randn((T, H), device=dev).bfloat16()
+    (t_sd, t_bc), _ = _time_calls(
+        [lambda: ep.ep_dispatch(x, idx, w, lay, dtype="fp8", recv_capacity=cap, out=d8,
+                                cumulative_recv_stats=stats),
+         lambda: ep.ep_combine(y, lay, idx, w, out=o, bias0=b0, bias1=b1)], reps, stream)
+    b_bc = N * H * 2 + T * H * 2 * 3 + meta
+    out["bias_stats"] = {"dispatch_with_stats_us": rnd(t_sd), "combine_with_two_biases_us": rnd(t_bc),
+                         "combine_with_two_biases_frac": frac(b_bc, t_bc), "plain_combine_us": rnd(t_c)}
+    assert lay.errors() == 0 and xl.errors() == 0, (lay.errors(), xl.errors())
+    return out
 
 
 def run_e2e(args, cfg, inp, y_np, cap, dev, world):
@@ -462,6 +563,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=W.HEADLINE, choices=list(W.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-next-rows", action="store_true",
+                    help="skip the secondary timings of the next rows (cached layout, packed, expanded, bias)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
     args.steps = max(1, args.steps)
