@@ -507,51 +507,77 @@ def run_next_rows(cfg, x, idx, w, y, cap, lay, peak, reps=200):
 
 
 def run_e2e(args, cfg, inp, y_np, cap, dev, world):
-    """The same step through the public binding with host buffers: copy the
-    step's inputs from pinned memory, run the path, copy the result back."""
+    """The same step through the public binding with host buffers: every
+    step copies its inputs in from pinned memory, runs the path and copies
+    the combined rows back.  As a serving loop would, it pipelines steps:
+    the inputs go in on one stream into double-buffered device inputs, the
+    path runs on a second, the result comes back on a third, so one step's
+    read-back overlaps the next step's upload (the two directions of the
+    host link)."""
     import combine_ep_get_layout_gb300 as ep
     h_x = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
     h_idx = torch.from_numpy(inp["topk_idx"]).pin_memory()
     h_w = torch.from_numpy(inp["topk_weights"]).pin_memory()
     h_y = torch.from_numpy(y_np.view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_out = torch.empty((cfg.num_tokens, cfg.hidden), dtype=torch.bfloat16).pin_memory()
-    d_x, d_idx, d_w, d_y = (torch.empty_like(t, device=dev) for t in (h_x, h_idx, h_w, h_y))
+    h_in = (h_x, h_idx, h_w, h_y)
+    h_out = [torch.empty((cfg.num_tokens, cfg.hidden), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    d_in = [[torch.empty_like(t, device=dev) for t in h_in] for _ in range(2)]
+    d_out = [torch.empty((cfg.num_tokens, cfg.hidden), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     lay = ep.Layout.empty(cfg.num_tokens, cfg.num_experts, cfg.num_ranks, dev)
     disp = None
-    d_out = torch.empty((cfg.num_tokens, cfg.hidden), dtype=torch.bfloat16, device=dev)
     dtype = "fp8" if cfg.fp8 else "bf16"
+    s_in, s_run, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_ready, ran, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    state = {"i": 0}
 
     def step():
         nonlocal disp
-        d_x.copy_(h_x, non_blocking=True)
-        d_idx.copy_(h_idx, non_blocking=True)
-        d_w.copy_(h_w, non_blocking=True)
-        d_y.copy_(h_y, non_blocking=True)
-        ep.ep_get_layout(d_idx, cfg.num_experts, cfg.num_ranks, layout=lay)
-        disp = ep.ep_dispatch(d_x, d_idx, d_w, lay, dtype=dtype, recv_capacity=cap, out=disp)
-        ep.ep_combine(d_y, lay, d_idx, d_w, out=d_out)
-        h_out.copy_(d_out, non_blocking=True)
+        i = state["i"]
+        b = i % 2
+        d_x, d_idx, d_w, d_y = d_in[b]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ran[b])      # the run two steps back has read these inputs
+            for d, h in zip(d_in[b], h_in):
+                d.copy_(h, non_blocking=True)
+            in_ready[b].record(s_in)
+        with torch.cuda.stream(s_run):
+            s_run.wait_event(in_ready[b])
+            if i >= 2:
+                s_run.wait_event(out_done[b])  # the read-back two steps back has read d_out[b]
+            ep.ep_get_layout(d_idx, cfg.num_experts, cfg.num_ranks, layout=lay, stream=s_run)
+            disp = ep.ep_dispatch(d_x, d_idx, d_w, lay, dtype=dtype, recv_capacity=cap, out=disp, stream=s_run)
+            ep.ep_combine(d_y, lay, d_idx, d_w, out=d_out[b], stream=s_run)
+            ran[b].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ran[b])
+            h_out[b].copy_(d_out[b], non_blocking=True)
+            out_done[b].record(s_out)
+        state["i"] = i + 1
 
     steps = max(10, args.steps // 20)
     for _ in range(3):
         step()
     torch.cuda.synchronize()
-    s = torch.cuda.current_stream(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
-    e0.record(s)
+    torch.cuda.synchronize()
+    e0.record(s_in)
     for _ in range(steps):
         step()
-    e1.record(s)
+    s_out.wait_event(ran[(state["i"] - 1) % 2])
+    e1.record(s_out)
     torch.cuda.synchronize()
     barrier(world)
     us = max_over_ranks(e0.elapsed_time(e1) / steps * 1e3, world)
-    h2d = sum(t.numel() * t.element_size() for t in (h_x, h_idx, h_w, h_y))
-    d2h = h_out.numel() * h_out.element_size()
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = h_out[0].numel() * h_out[0].element_size()
     return {"value": round(us, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
             "note": "inputs x, topk_idx, topk_weights and the expert output y copied in, "
-                    "the combined rows copied out, every step"}
+                    "the combined rows copied out, every step; steps pipelined over three "
+                    "streams (upload, path, read-back)"}
 
 
 def main(argv=None):
