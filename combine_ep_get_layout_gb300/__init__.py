@@ -27,6 +27,7 @@ from ._native import (EP_ERRBIT_BAD_INDEX, EP_ERRBIT_CAPACITY,  # noqa: F401
 
 __all__ = ["EPError", "Layout", "Dispatched", "ep_layout_workspace_bytes",
            "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch", "ep_dispatch_ex",
+           "ep_get_layout_and_dispatch",
            "ep_combine", "ep_combine_ex", "ep_fp8_packed_row_bytes", "ExpandedLayout",
            "ep_expanded_layout_workspace_bytes", "ep_get_layout_expanded",
            "ep_dispatch_expanded", "ep_combine_expanded", "library_path"]
@@ -180,28 +181,14 @@ _DTYPES = {"bf16": N.EP_DTYPE_BF16, "fp8": N.EP_DTYPE_FP8_E4M3,
            "fp8_packed": N.EP_DTYPE_FP8_E4M3_PACKED}
 
 
-def ep_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: Optional[torch.Tensor],
-                layout: Layout, dtype: str = "bf16", recv_capacity: Optional[int] = None,
-                out: Optional[Dispatched] = None, metadata: bool = True,
-                cumulative_recv_stats: Optional[torch.Tensor] = None,
-                stream=None) -> Dispatched:
-    """Scatter rows of ``x`` (bf16 [T, H]) to their received slots.
-
-    ``dtype`` is "bf16", "fp8" (e4m3 rows + a separate scale array) or
-    "fp8_packed" (codes, scales and padding in one uint8 row of
-    ``ep_fp8_packed_row_bytes(H)`` bytes).  Without ``recv_capacity`` the
-    buffers are sized T * min(K, R), which needs no read-back of the layout.
-    ``cumulative_recv_stats`` (uint32 [E]) is accumulated in place.  The
-    plain C entry point ep_dispatch serves the options it has; the others go
-    through ep_dispatch_ex.
-    """
+def _dispatch_outputs(x, topk_idx, topk_weights, E, R, code, recv_capacity, out, metadata,
+                      cumulative_recv_stats):
+    """Checks the dispatch arguments and allocates the outputs not given."""
     _want(x, "x", torch.bfloat16)
     dev = x.device
     _want(topk_idx, "topk_idx", torch.int64, dev)
     T, H = x.shape
     K = topk_idx.shape[1]
-    E, R = layout.num_experts, layout.num_ranks
-    code = _DTYPES[dtype]
     fp8 = code != N.EP_DTYPE_BF16
     packed = code == N.EP_DTYPE_FP8_E4M3_PACKED
     if recv_capacity is None:
@@ -230,19 +217,49 @@ def ep_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: Optional[
         if cumulative_recv_stats.dtype not in (torch.int32, torch.uint32) or \
                 cumulative_recv_stats.numel() != E or not cumulative_recv_stats.is_cuda:
             raise ValueError("cumulative_recv_stats must be a 32-bit CUDA tensor of num_experts entries")
+    return out, recv_capacity
+
+
+def _dispatch_args(x, topk_idx, topk_weights, E, R, st, code, out, recv_capacity, stats):
+    T, H = x.shape
+    return N.ep_dispatch_args_t(
+        x.data_ptr(), T, H, topk_idx.data_ptr(),
+        None if topk_weights is None else topk_weights.data_ptr(), topk_idx.shape[1], E, R,
+        C.pointer(st), code, out.recv_x.data_ptr(),
+        None if out.recv_x_scales is None else out.recv_x_scales.data_ptr(),
+        None if out.recv_src_idx is None else out.recv_src_idx.data_ptr(),
+        None if out.recv_topk_idx is None else out.recv_topk_idx.data_ptr(),
+        None if out.recv_topk_weights is None else out.recv_topk_weights.data_ptr(),
+        recv_capacity, None if stats is None else stats.data_ptr())
+
+
+def ep_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: Optional[torch.Tensor],
+                layout: Layout, dtype: str = "bf16", recv_capacity: Optional[int] = None,
+                out: Optional[Dispatched] = None, metadata: bool = True,
+                cumulative_recv_stats: Optional[torch.Tensor] = None,
+                stream=None) -> Dispatched:
+    """Scatter rows of ``x`` (bf16 [T, H]) to their received slots.
+
+    ``dtype`` is "bf16", "fp8" (e4m3 rows + a separate scale array) or
+    "fp8_packed" (codes, scales and padding in one uint8 row of
+    ``ep_fp8_packed_row_bytes(H)`` bytes).  Without ``recv_capacity`` the
+    buffers are sized T * min(K, R), which needs no read-back of the layout.
+    ``cumulative_recv_stats`` (uint32 [E]) is accumulated in place.  The
+    plain C entry point ep_dispatch serves the options it has; the others go
+    through ep_dispatch_ex.
+    """
+    E, R = layout.num_experts, layout.num_ranks
+    code = _DTYPES[dtype]
+    out, recv_capacity = _dispatch_outputs(x, topk_idx, topk_weights, E, R, code, recv_capacity, out,
+                                           metadata, cumulative_recv_stats)
+    dev = x.device
+    T, H = x.shape
+    K = topk_idx.shape[1]
     st = layout.c_struct()
     lib = N.load()
-    if packed or cumulative_recv_stats is not None:
-        args = N.ep_dispatch_args_t(
-            x.data_ptr(), T, H, topk_idx.data_ptr(),
-            None if topk_weights is None else topk_weights.data_ptr(), K, E, R,
-            C.pointer(st), code, out.recv_x.data_ptr(),
-            None if out.recv_x_scales is None else out.recv_x_scales.data_ptr(),
-            None if out.recv_src_idx is None else out.recv_src_idx.data_ptr(),
-            None if out.recv_topk_idx is None else out.recv_topk_idx.data_ptr(),
-            None if out.recv_topk_weights is None else out.recv_topk_weights.data_ptr(),
-            recv_capacity,
-            None if cumulative_recv_stats is None else cumulative_recv_stats.data_ptr())
+    if code == N.EP_DTYPE_FP8_E4M3_PACKED or cumulative_recv_stats is not None:
+        args = _dispatch_args(x, topk_idx, topk_weights, E, R, st, code, out, recv_capacity,
+                              cumulative_recv_stats)
         _check(lib.ep_dispatch_ex(C.byref(args), _stream(stream, dev)), "ep_dispatch_ex")
     else:
         _check(lib.ep_dispatch(
@@ -251,6 +268,34 @@ def ep_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: Optional[
             _ptr(out.recv_topk_idx), _ptr(out.recv_topk_weights), recv_capacity,
             _stream(stream, dev)), "ep_dispatch")
     return out
+
+
+def ep_get_layout_and_dispatch(x: torch.Tensor, topk_idx: torch.Tensor,
+                               topk_weights: Optional[torch.Tensor], num_experts: int, num_ranks: int,
+                               layout: Optional[Layout] = None, dtype: str = "fp8",
+                               recv_capacity: Optional[int] = None, out: Optional[Dispatched] = None,
+                               metadata: bool = True,
+                               cumulative_recv_stats: Optional[torch.Tensor] = None,
+                               stream=None, work_counters: bool = True):
+    """ep_get_layout then ep_dispatch as one call: with fp8 rows the
+    dispatch loads and casts its first rows while the layout kernel still
+    runs.  Returns (layout, dispatched), both as the two calls give them."""
+    T = topk_idx.shape[0]
+    dev = x.device
+    if layout is None:
+        layout = Layout.empty(T, num_experts, num_ranks, dev, work_counters)
+    elif (layout.num_tokens, layout.num_experts, layout.num_ranks) != (T, num_experts, num_ranks):
+        raise ValueError("layout was allocated for other sizes")
+    code = _DTYPES[dtype]
+    out, recv_capacity = _dispatch_outputs(x, topk_idx, topk_weights, num_experts, num_ranks, code,
+                                           recv_capacity, out, metadata, cumulative_recv_stats)
+    st = layout.c_struct()
+    args = _dispatch_args(x, topk_idx, topk_weights, num_experts, num_ranks, st, code, out,
+                          recv_capacity, cumulative_recv_stats)
+    _check(N.load().ep_get_layout_and_dispatch(
+        C.byref(args), _ptr(layout.workspace), layout.workspace.numel(), _stream(stream, dev)),
+        "ep_get_layout_and_dispatch")
+    return layout, out
 
 
 ep_dispatch_ex = ep_dispatch

@@ -116,6 +116,7 @@ SIGNATURES = {
     "ep_combine": (_i, [_p, _i, _i, _LP, _i, _i, _p, _p, _i, _i, _p, _p]),
     "ep_fp8_packed_row_bytes": (_sz, [_i]),
     "ep_dispatch_ex": (_i, [C.POINTER(ep_dispatch_args_t), _p]),
+    "ep_get_layout_and_dispatch": (_i, [C.POINTER(ep_dispatch_args_t), _p, _sz, _p]),
     "ep_combine_ex": (_i, [C.POINTER(ep_combine_args_t), _p]),
     "ep_expanded_layout_workspace_bytes": (_sz, [_i, _i]),
     "ep_get_layout_expanded": (_i, [_p, _i, _i, _i, _i, C.POINTER(ep_expanded_layout_t), _p, _sz, _p]),

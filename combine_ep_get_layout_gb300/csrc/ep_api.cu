@@ -110,6 +110,65 @@ ep_status_t check_ptr(const char *fn, const char *name, const void *p, size_t al
     if (_s != EP_OK) return _s;          \
   } while (0)
 
+// Validates the arguments of a rank-path dispatch (host only) and fills `a`.
+ep_status_t dispatch_args(const char *fn, const ep_dispatch_args_t *args, DispatchArgs &a) {
+  if (args == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: args is NULL", fn);
+  const ep_dispatch_args_t &x = *args;
+  if (x.num_tokens < 0) return fail(EP_ERR_INVALID_ARG, "%s: num_tokens=%d < 0", fn, x.num_tokens);
+  if (x.dtype != EP_DTYPE_BF16 && x.dtype != EP_DTYPE_FP8_E4M3 && x.dtype != EP_DTYPE_FP8_E4M3_PACKED)
+    return fail(EP_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)x.dtype);
+  const bool fp8 = x.dtype != EP_DTYPE_BF16;
+  const bool packed = x.dtype == EP_DTYPE_FP8_E4M3_PACKED;
+  if (x.hidden < 1) return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d < 1", fn, x.hidden);
+  if (x.hidden > EP_MAX_HIDDEN)
+    return fail(EP_ERR_UNSUPPORTED, "%s: hidden=%d > %d", fn, x.hidden, EP_MAX_HIDDEN);
+  if (x.hidden % (fp8 ? EP_FP8_GROUP : 8) != 0)
+    return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d is not a multiple of %d", fn, x.hidden,
+                fp8 ? EP_FP8_GROUP : 8);
+  EP_CHECK(check_routing_sizes(fn, x.num_topk, x.num_experts, x.num_ranks));
+  if (x.recv_capacity < 0) return fail(EP_ERR_INVALID_ARG, "%s: recv_capacity=%d < 0", fn, x.recv_capacity);
+  const bool any = x.num_tokens > 0;
+  const bool rows = x.recv_capacity > 0;
+  EP_CHECK(check_ptr(fn, "x", x.x, 16, any));
+  EP_CHECK(check_ptr(fn, "topk_idx", x.topk_idx, 8, any));
+  if (x.layout == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: layout is NULL", fn);
+  EP_CHECK(check_ptr(fn, "layout.token_slot", x.layout->token_slot, 4, any));
+  EP_CHECK(check_ptr(fn, "layout.error_word", x.layout->error_word, 4, true));
+  EP_CHECK(check_ptr(fn, "layout.work_counters", x.layout->work_counters, 16, false));
+  EP_CHECK(check_ptr(fn, "recv_x", x.recv_x, 16, rows));
+  EP_CHECK(check_ptr(fn, "recv_x_scales", x.recv_x_scales, 4, fp8 && !packed && rows));
+  EP_CHECK(check_ptr(fn, "recv_src_idx", x.recv_src_idx, 4, false));
+  EP_CHECK(check_ptr(fn, "recv_topk_idx", x.recv_topk_idx, 4, false));
+  EP_CHECK(check_ptr(fn, "recv_topk_weights", x.recv_topk_weights, 4, false));
+  EP_CHECK(check_ptr(fn, "topk_weights", x.topk_weights, 4, any && x.recv_topk_weights != nullptr));
+  EP_CHECK(check_ptr(fn, "cumulative_recv_stats", x.cumulative_recv_stats, 4, false));
+  a.x = static_cast<const uint16_t *>(x.x);
+  a.num_tokens = x.num_tokens;
+  a.hidden = x.hidden;
+  a.num_topk = x.num_topk;
+  a.num_experts = x.num_experts;
+  a.num_ranks = x.num_ranks;
+  a.topk_idx = x.topk_idx;
+  a.topk_weights = x.topk_weights;
+  a.token_slot = x.layout->token_slot;
+  a.error_word = x.layout->error_word;
+  a.expanded = false;
+  a.expert_offset = nullptr;
+  a.num_rows_per_expert = nullptr;
+  a.zero_padding = false;
+  a.fp8 = fp8;
+  a.packed_row_bytes = packed ? (int)fp8_packed_row_bytes(x.hidden) : 0;
+  a.work_counters = x.layout->work_counters;  // words 0-1: dispatch
+  a.recv_x = x.recv_x;
+  a.recv_x_scales = packed ? nullptr : x.recv_x_scales;
+  a.recv_src_idx = x.recv_src_idx;
+  a.recv_topk_idx = x.recv_topk_idx;
+  a.recv_topk_weights = x.recv_topk_weights;
+  a.recv_capacity = x.recv_capacity;
+  a.recv_stats = x.cumulative_recv_stats;
+  return EP_OK;
+}
+
 }  // namespace
 }  // namespace ep
 
@@ -153,64 +212,35 @@ size_t ep_fp8_packed_row_bytes(int hidden) {
 }
 
 ep_status_t ep_dispatch_ex(const ep_dispatch_args_t *args, ep_stream_t stream) {
-  static const char *fn = "ep_dispatch";
   clear_error();
-  if (args == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: args is NULL", fn);
-  const ep_dispatch_args_t &x = *args;
-  if (x.num_tokens < 0) return fail(EP_ERR_INVALID_ARG, "%s: num_tokens=%d < 0", fn, x.num_tokens);
-  if (x.dtype != EP_DTYPE_BF16 && x.dtype != EP_DTYPE_FP8_E4M3 && x.dtype != EP_DTYPE_FP8_E4M3_PACKED)
-    return fail(EP_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)x.dtype);
-  const bool fp8 = x.dtype != EP_DTYPE_BF16;
-  const bool packed = x.dtype == EP_DTYPE_FP8_E4M3_PACKED;
-  if (x.hidden < 1) return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d < 1", fn, x.hidden);
-  if (x.hidden > EP_MAX_HIDDEN)
-    return fail(EP_ERR_UNSUPPORTED, "%s: hidden=%d > %d", fn, x.hidden, EP_MAX_HIDDEN);
-  if (x.hidden % (fp8 ? EP_FP8_GROUP : 8) != 0)
-    return fail(EP_ERR_INVALID_ARG, "%s: hidden=%d is not a multiple of %d", fn, x.hidden,
-                fp8 ? EP_FP8_GROUP : 8);
-  EP_CHECK(check_routing_sizes(fn, x.num_topk, x.num_experts, x.num_ranks));
-  if (x.recv_capacity < 0) return fail(EP_ERR_INVALID_ARG, "%s: recv_capacity=%d < 0", fn, x.recv_capacity);
-  const bool any = x.num_tokens > 0;
-  const bool rows = x.recv_capacity > 0;
-  EP_CHECK(check_ptr(fn, "x", x.x, 16, any));
-  EP_CHECK(check_ptr(fn, "topk_idx", x.topk_idx, 8, any));
-  if (x.layout == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: layout is NULL", fn);
-  EP_CHECK(check_ptr(fn, "layout.token_slot", x.layout->token_slot, 4, any));
-  EP_CHECK(check_ptr(fn, "layout.error_word", x.layout->error_word, 4, true));
-  EP_CHECK(check_ptr(fn, "layout.work_counters", x.layout->work_counters, 16, false));
-  EP_CHECK(check_ptr(fn, "recv_x", x.recv_x, 16, rows));
-  EP_CHECK(check_ptr(fn, "recv_x_scales", x.recv_x_scales, 4, fp8 && !packed && rows));
-  EP_CHECK(check_ptr(fn, "recv_src_idx", x.recv_src_idx, 4, false));
-  EP_CHECK(check_ptr(fn, "recv_topk_idx", x.recv_topk_idx, 4, false));
-  EP_CHECK(check_ptr(fn, "recv_topk_weights", x.recv_topk_weights, 4, false));
-  EP_CHECK(check_ptr(fn, "topk_weights", x.topk_weights, 4, any && x.recv_topk_weights != nullptr));
-  EP_CHECK(check_ptr(fn, "cumulative_recv_stats", x.cumulative_recv_stats, 4, false));
   DispatchArgs a;
-  a.x = static_cast<const uint16_t *>(x.x);
-  a.num_tokens = x.num_tokens;
-  a.hidden = x.hidden;
-  a.num_topk = x.num_topk;
-  a.num_experts = x.num_experts;
-  a.num_ranks = x.num_ranks;
-  a.topk_idx = x.topk_idx;
-  a.topk_weights = x.topk_weights;
-  a.token_slot = x.layout->token_slot;
-  a.error_word = x.layout->error_word;
-  a.expanded = false;
-  a.expert_offset = nullptr;
-  a.num_rows_per_expert = nullptr;
-  a.zero_padding = false;
-  a.fp8 = fp8;
-  a.packed_row_bytes = packed ? (int)fp8_packed_row_bytes(x.hidden) : 0;
-  a.work_counters = x.layout->work_counters;  // words 0-1: dispatch
-  a.recv_x = x.recv_x;
-  a.recv_x_scales = packed ? nullptr : x.recv_x_scales;
-  a.recv_src_idx = x.recv_src_idx;
-  a.recv_topk_idx = x.recv_topk_idx;
-  a.recv_topk_weights = x.recv_topk_weights;
-  a.recv_capacity = x.recv_capacity;
-  a.recv_stats = x.cumulative_recv_stats;
+  EP_CHECK(dispatch_args("ep_dispatch", args, a));
   return launch_dispatch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ep_status_t ep_get_layout_and_dispatch(const ep_dispatch_args_t *args, void *workspace, size_t workspace_bytes,
+                                       ep_stream_t stream) {
+  static const char *fn = "ep_get_layout_and_dispatch";
+  clear_error();
+  DispatchArgs a;
+  EP_CHECK(dispatch_args(fn, args, a));
+  const ep_layout_t *layout = args->layout;
+  const bool any = a.num_tokens > 0;
+  EP_CHECK(check_ptr(fn, "layout.num_tokens_per_expert", layout->num_tokens_per_expert, 4, true));
+  EP_CHECK(check_ptr(fn, "layout.num_tokens_per_rank", layout->num_tokens_per_rank, 4, true));
+  EP_CHECK(check_ptr(fn, "layout.rank_prefix", layout->rank_prefix, 4, true));
+  EP_CHECK(check_ptr(fn, "layout.is_token_in_rank", layout->is_token_in_rank, 16, any));
+  EP_CHECK(check_ptr(fn, "layout.token_slot", layout->token_slot, 16, any));
+  EP_CHECK(check_ptr(fn, "workspace", workspace, 16, true));
+  const size_t need = layout_workspace_bytes(a.num_tokens, a.num_experts, a.num_ranks);
+  if (workspace_bytes < need)
+    return fail(EP_ERR_INVALID_ARG, "%s: workspace_bytes=%zu < %zu needed", fn, workspace_bytes, need);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  EP_CHECK(launch_layout(args->topk_idx, a.num_tokens, a.num_topk, a.num_experts, a.num_ranks, *layout, workspace, s));
+  // The kernel ahead of the dispatch is the layout, which writes nothing the
+  // dispatch reads before its wait; so its first rows load and cast early.
+  a.early_rows = kEarlyRows;
+  return launch_dispatch(a, s);
 }
 
 ep_status_t ep_dispatch(const void *x, int num_tokens, int hidden, const int64_t *topk_idx,

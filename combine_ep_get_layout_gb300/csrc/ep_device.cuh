@@ -266,9 +266,14 @@ __device__ __forceinline__ void retire_tokens(const TokenSource &ts, bool &drain
 // the first too: a block that starts late (its SM still busy with the
 // previous kernel) then owns no token yet.  `drained`: the drawing thread's
 // state, false at the start.
-__device__ __forceinline__ int draw_token(const TokenSource &ts, int i, bool &drained) {
+//
+// `head` > 0 (ticket mode): the block's first `head` tokens are its own
+// stripe (blockIdx.x + i * gridDim.x, i < head) and tickets number the
+// tokens after head * gridDim.x, so those first draws touch no counter.
+__device__ __forceinline__ int draw_token(const TokenSource &ts, int i, bool &drained, int head = 0) {
   if (drained) return -1;
-  const int t = ts.ticket == nullptr ? (int)blockIdx.x + i * (int)gridDim.x : (int)atomicAdd(ts.ticket, 1u);
+  const int t = (ts.ticket == nullptr || i < head) ? (int)blockIdx.x + i * (int)gridDim.x
+                                                   : head * (int)gridDim.x + (int)atomicAdd(ts.ticket, 1u);
   if (t < ts.T) return t;
   retire_tokens(ts, drained);
   return -1;

@@ -61,6 +61,7 @@ struct DispatchParams {
   uint32_t out_stride;     // fp8 output row, H rounded up to 128
   uint32_t scale_stride;   // fp8 scales of one row, groups*4 rounded up to 16
   TokenSource tokens;      // the order in which blocks take tokens
+  int early;               // fp8 kernel: rows loaded and cast before the wait for the previous kernel
 };
 
 // Token ids travel from the loading thread to the other roles of a block
@@ -76,8 +77,9 @@ constexpr int kTokTimedOut = INT_MIN + 1;  // wait_token gave up
 // tokens are exhausted it records -1 and completes the stage's phase with a
 // plain arrival instead, so every index has a phase.  One thread.
 __device__ __forceinline__ void issue_token(const DispatchParams &p, unsigned char *stages, uint64_t *full,
-                                            volatile int *s_tok, int idx, bool &drained, uint64_t policy) {
-  const int t = draw_token(p.tokens, idx, drained);
+                                            volatile int *s_tok, int idx, bool &drained, uint64_t policy,
+                                            int head = 0) {
+  const int t = draw_token(p.tokens, idx, drained, head);
   const int s = idx % p.stages;
   s_tok[idx % kTokRing] = t;
   if (t < 0) {
@@ -463,7 +465,13 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
     fence_proxy_async_smem();
   }
   __syncthreads();
-  griddep_wait();
+  // With p.early > 0 the previous kernel on the stream (the layout) writes
+  // nothing this kernel reads before its wait: the loader brings in the rows
+  // of its first p.early tokens (its own stripe) and the casters cast them
+  // while the layout is still running; the loader waits before its first
+  // ticket, the storer before it reads the layout.  The casters touch no
+  // global memory.
+  if (p.early == 0) griddep_wait();
   griddep_launch_dependents();
 
   int issued = 0;        // loader lane 0: token indices drawn (loads and the end)
@@ -471,6 +479,7 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t policy = policy_evict_first();
+      bool waited = p.early == 0;
       for (int i = 0; !drained && !*s_abort; ++i) {
         const int s = i % S;
         if (i >= S && !mbar_wait_bounded(&empty_in[s], (uint32_t)(i / S - 1) & 1u)) {
@@ -478,12 +487,19 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
           set_error(p.error_word, EP_ERRBIT_TIMEOUT);
           break;
         }
-        issue_token(p, in, full_in, s_tok, i, drained, policy);
+        // the first draw that may touch the counter (a ticket, or the end)
+        if (!waited && (i >= p.early || (long)blockIdx.x + (long)i * gridDim.x >= p.T)) {
+          griddep_wait();
+          waited = true;
+        }
+        issue_token(p, in, full_in, s_tok, i, drained, policy, p.early);
         issued = i + 1;
       }
+      if (!waited) griddep_wait();
       retire_tokens(p.tokens, drained);
     }
   } else if (warp == 1) {
+    if (p.early > 0) griddep_wait();
     const bool scale_bulk = p.scale_stride == (uint32_t)p.groups * 4u &&
                             (reinterpret_cast<uintptr_t>(p.recv_x_scales) & 15u) == 0;
     for (int i = 0; !*s_abort; ++i) {
@@ -839,6 +855,7 @@ ep_status_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream) {
   p.tokens.ticket = a.work_counters;
   p.tokens.done = a.work_counters != nullptr ? a.work_counters + 1 : nullptr;
   p.tokens.T = a.num_tokens;
+  p.early = a.early_rows;
   ep_status_t st = EP_OK;
   if (a.num_tokens > 0) {
     // packed rows are only built by the warp-specialised kernel

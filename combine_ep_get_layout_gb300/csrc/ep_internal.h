@@ -75,7 +75,13 @@ struct DispatchArgs {
   float *recv_topk_weights;
   int recv_capacity;
   uint32_t *recv_stats;  // [E] or null
+  // fp8 rows: tokens per block loaded and cast before the wait for the
+  // previous kernel on the stream; only when that kernel writes none of x
+  int early_rows = 0;
 };
+// early_rows of ep_get_layout_and_dispatch (the input stages and the output
+// buffers of the warp-specialised kernel hold up to 5 tokens)
+constexpr int kEarlyRows = 3;
 ep_status_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream);
 
 // ---- combine (ep_combine.cu)

@@ -281,6 +281,27 @@ typedef struct {
 ep_status_t ep_dispatch_ex(const ep_dispatch_args_t *args, ep_stream_t stream);
 
 /*
+ * ep_get_layout of args->topk_idx into *args->layout, then ep_dispatch_ex
+ * with the same arguments, as one call: the notify (count and exchange) and
+ * the scatter of TileScale PR #68 issued together (same page, commit
+ * messages fusing the layout back into the dispatch).  The work is the same
+ * two launches, overlapped: the kernel ahead of the dispatch is known to be
+ * the layout, which writes nothing the dispatch reads first, so with fp8
+ * rows each dispatch block loads and casts the rows of its first tokens
+ * while the layout still runs, and waits for it only to store them.  Every
+ * output of both calls is written, identical to the two calls.
+ *   args       as for ep_dispatch_ex; every array of *args->layout is
+ *              written (as ep_get_layout), so its token_slot and
+ *              is_token_in_rank must be 16-byte aligned.
+ *   workspace  ep_layout_workspace_bytes(T, E, R) bytes, as for
+ *              ep_get_layout (the same buffer serves both calls).
+ * Errors: those of ep_get_layout and ep_dispatch_ex, checked before any
+ * launch.
+ */
+ep_status_t ep_get_layout_and_dispatch(const ep_dispatch_args_t *args, void *workspace, size_t workspace_bytes,
+                                       ep_stream_t stream);
+
+/*
  * Combine: the local reduce of TileScale PR #68 (PR summary: one block per
  * source token reduces the rows stored back for it).  On one GPU the
  * store-back slot comm_x[rank][src_token] is the received row

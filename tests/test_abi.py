@@ -323,3 +323,23 @@ def test_work_counters_must_be_16_byte_aligned(lib):
     xd, _keep2 = _xdargs(lay=xl)
     name, msg = _status(lib, lib.ep_dispatch_expanded(C.byref(xd), None))
     assert name == "EP_ERR_INVALID_ARG" and "work_counters" in msg
+
+
+def test_layout_and_dispatch_rejects(lib):
+    """ep_get_layout_and_dispatch checks the arguments of both calls, and its
+    workspace against ep_layout_workspace_bytes, before any launch."""
+    need = lib.ep_layout_workspace_bytes(100, 16, 4)
+    args, _keep = _dargs()
+    name, msg = _status(lib, lib.ep_get_layout_and_dispatch(C.byref(args), FAKE, need - 16, None))
+    assert name == "EP_ERR_INVALID_ARG" and "workspace_bytes" in msg
+    name, msg = _status(lib, lib.ep_get_layout_and_dispatch(C.byref(args), None, need, None))
+    assert name == "EP_ERR_INVALID_ARG" and "workspace is NULL" in msg
+    name, msg = _status(lib, lib.ep_get_layout_and_dispatch(C.byref(args), MISALIGNED, need, None))
+    assert name == "EP_ERR_INVALID_ARG" and "workspace" in msg
+    args.layout.contents.rank_prefix = None
+    name, msg = _status(lib, lib.ep_get_layout_and_dispatch(C.byref(args), FAKE, need, None))
+    assert name == "EP_ERR_INVALID_ARG" and "rank_prefix" in msg
+    args2, _keep2 = _dargs(hidden=100, dtype=1)
+    name, msg = _status(lib, lib.ep_get_layout_and_dispatch(C.byref(args2), FAKE, need, None))
+    assert name == "EP_ERR_INVALID_ARG" and "hidden" in msg
+    assert _status(lib, lib.ep_get_layout_and_dispatch(None, FAKE, need, None))[0] == "EP_ERR_INVALID_ARG"

@@ -1,0 +1,178 @@
+"""ep_get_layout_and_dispatch against the oracle (GPU): the layout and the
+dispatch issued as one call (TileScale PR #68, commit messages fusing the
+layout back into the dispatch), with the fp8 dispatch loading and casting its
+first rows while the layout kernel runs, must give exactly what
+ep_get_layout followed by ep_dispatch give -- every layout array, every
+received row and its metadata, bit for bit -- for fp8, packed fp8 and bf16
+rows, ragged and degenerate sizes, and call after call."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+ep = pytest.importorskip("combine_ep_get_layout_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from combine_ep_get_layout_gb300 import build
+    build.build()
+
+
+import gpu_util as U  # noqa: E402
+
+
+def _routing(T, K, E, seed, p_mask=0.1, bad=0.0):
+    rng = np.random.default_rng(seed)
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :K] if T else np.zeros((0, K), np.int64)
+    idx = np.where(rng.random((T, K)) < p_mask, -1, idx).astype(np.int64)
+    if bad:
+        m = rng.random((T, K)) < bad
+        idx = np.where(m, rng.choice([-3, E, E + 5], size=(T, K)), idx).astype(np.int64)
+    w = rng.random((T, K)).astype(np.float32)
+    return idx, w, rng
+
+
+def _run(x, idx, w, E, R, dtype, cap, stats=None, work_counters=True, layout=None, out=None):
+    d_idx = torch.from_numpy(idx).to(U.dev())
+    lay, d = ep.ep_get_layout_and_dispatch(
+        U.to_dev_bf16(x), d_idx, torch.from_numpy(w).to(U.dev()), E, R, layout=layout, dtype=dtype,
+        recv_capacity=cap, out=out, cumulative_recv_stats=stats, work_counters=work_counters)
+    torch.cuda.synchronize()
+    return lay, d
+
+
+def _check(x, idx, w, E, R, dtype, cap=None, rows=None, stats=False, work_counters=True):
+    T = idx.shape[0]
+    lo = oracle.get_layout(idx, E, R)
+    N = int(lo["rank_prefix"][R])
+    cap = max(N, 1) if cap is None else cap
+    mode = {"bf16": False, "fp8": True, "fp8_packed": "packed"}[dtype]
+    st_o = np.zeros(E, np.uint32) if stats else None
+    o = oracle.dispatch(x, idx, w, E, R, lo["token_slot"], mode, cap, stats=st_o)
+    st = torch.zeros(E, dtype=torch.int32, device=U.dev()) if stats else None
+    lay, d = _run(x, idx, w, E, R, dtype, cap, stats=st, work_counters=work_counters)
+    g = U.layout_np(lay)
+    for k in U.LAYOUT_KEYS:  # the error word is checked by the callers (dispatch adds its bits)
+        assert np.array_equal(g[k], lo[k]), k
+    if work_counters:
+        assert U.bits(lay.work_counters).tolist() == [0, 0, 0, 0]
+    n = min(N, cap)
+    sel = slice(0, n) if rows is None else rows
+    assert np.array_equal(U.bits(d.recv_x)[sel], o["recv_x"][sel])
+    assert np.array_equal(U.bits(d.recv_src_idx)[sel], o["recv_src_idx"][sel])
+    assert np.array_equal(U.bits(d.recv_topk_idx)[sel], o["recv_topk_idx"][sel])
+    assert np.array_equal(U.bits(d.recv_topk_weights)[sel].view(np.uint32),
+                          o["recv_topk_weights"][sel].view(np.uint32))
+    if dtype == "fp8":
+        assert np.array_equal(U.bits(d.recv_x_scales)[sel].view(np.uint32),
+                              o["recv_x_scales"][sel].view(np.uint32))
+    if stats:
+        assert np.array_equal(U.bits(st).view(np.uint32), st_o)
+    return lay, lo
+
+
+def test_headline_workload():
+    cfg = W.CONFIGS["fp8_8192x7168_top8_256e"]
+    inp = W.make(cfg)
+    _check(inp["x"], inp["topk_idx"], inp["topk_weights"], cfg.num_experts, cfg.num_ranks, "fp8")
+
+
+CASES = [
+    # name, T, H, K, E, R, dtype, kw
+    ("fp8_small", 300, 512, 6, 64, 8, "fp8", {}),
+    ("fp8_T1", 1, 256, 4, 16, 4, "fp8", {}),
+    ("fp8_T5", 5, 128, 2, 8, 2, "fp8", {}),
+    ("fp8_R1", 700, 256, 4, 16, 1, "fp8", {}),
+    ("fp8_R5_scalar_slots", 900, 384, 6, 20, 5, "fp8", {}),
+    ("fp8_R64_two_ranks_per_lane", 1500, 256, 8, 128, 64, "fp8", {}),
+    ("fp8_K32", 400, 256, 32, 64, 8, "fp8", {}),
+    ("fp8_bad_ids", 2000, 256, 6, 32, 8, "fp8", dict(bad=0.03)),
+    ("fp8_all_masked", 500, 256, 4, 16, 4, "fp8", dict(p_mask=1.0)),
+    ("packed_stats", 3000, 640, 5, 20, 5, "fp8_packed", {}),
+    ("fp8_stripes", 3000, 1024, 8, 64, 8, "fp8", dict(work_counters=False)),
+    ("bf16_rows", 1000, 256, 6, 64, 8, "bf16", {}),
+    ("fp8_T0", 0, 256, 4, 16, 4, "fp8", {}),
+    ("fp8_fewer_tokens_than_blocks", 37, 7168, 8, 256, 8, "fp8", {}),
+    ("fp8_about_3_tokens_per_block", 1900, 1024, 8, 64, 8, "fp8", {}),
+    ("fp8_stripes_few_tokens", 50, 512, 4, 16, 4, "fp8", dict(work_counters=False)),
+    ("fp8_19457_tokens", 19457, 256, 8, 64, 8, "fp8", {}),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_cases(case):
+    _, T, H, K, E, R, dtype, kw = case
+    wc = kw.pop("work_counters", True)
+    idx, w, rng = _routing(T, K, E, 7, **kw)
+    x = W.normal_bf16(rng, (T, H))
+    lay, lo = _check(x, idx, w, E, R, dtype, stats=(dtype == "fp8_packed"), work_counters=wc)
+    want = (oracle.BAD_INDEX if (idx < -1).any() or (idx >= E).any() else 0)
+    assert lay.errors() == want and lo["error"] == want
+
+
+def test_capacity_overflow():
+    T, H, K, E, R = 2000, 256, 6, 64, 8
+    idx, w, rng = _routing(T, K, E, 8)
+    x = W.normal_bf16(rng, (T, H))
+    lo = oracle.get_layout(idx, E, R)
+    cap = int(lo["rank_prefix"][R]) // 2
+    lay, _ = _check(x, idx, w, E, R, "fp8", cap=cap)
+    assert lay.errors() & ep.EP_ERRBIT_CAPACITY
+
+
+def test_many_tokens_few_columns():
+    """400 000 tokens of 128 columns: a sample of the rows and the whole
+    layout against the oracle."""
+    T, H, K, E, R = 400_000, 128, 2, 16, 4
+    idx, w, rng = _routing(T, K, E, 9)
+    x = W.normal_bf16(rng, (T, H))
+    _check(x, idx, w, E, R, "fp8", rows=np.sort(np.random.default_rng(0).choice(400_000, 3000, replace=False)))
+
+
+def test_large_workload():
+    """The 65536-token workload: the whole layout and a sample of the rows
+    against the oracle."""
+    cfg = W.CONFIGS["fp8_65536x7168_top8_256e"]
+    inp = W.make(cfg)
+    E, R = cfg.num_experts, cfg.num_ranks
+    idx, w, x = inp["topk_idx"], inp["topk_weights"], inp["x"]
+    lo = oracle.get_layout(idx, E, R)
+    N = int(lo["rank_prefix"][R])
+    lay, d = _run(x, idx, w, E, R, "fp8", N)
+    U.assert_layout_equal(U.layout_np(lay), lo)
+    toks = np.unique(np.random.default_rng(1).choice(cfg.num_tokens, 600, replace=False))
+    local, glob = U.subset_problem(toks, lo["token_slot"])
+    o = oracle.dispatch(x[toks], idx[toks], w[toks], E, R, local, True, len(glob))
+    n = len(glob)
+    assert np.array_equal(U.bits(d.recv_x)[glob], o["recv_x"][:n])
+    assert np.array_equal(U.bits(d.recv_x_scales)[glob].view(np.uint32), o["recv_x_scales"][:n].view(np.uint32))
+    assert np.array_equal(U.bits(d.recv_src_idx)[glob], toks[o["recv_src_idx"][:n]])
+
+
+def test_repeated_and_mixed_with_layout_kernel():
+    """Call after call on one layout and workspace, with plain ep_get_layout
+    calls in between: the work counters and the workspace stay reusable."""
+    T, H, K, E, R = 4096, 1024, 8, 64, 8
+    idx, w, rng = _routing(T, K, E, 10)
+    x = W.normal_bf16(rng, (T, H))
+    lo = oracle.get_layout(idx, E, R)
+    N = int(lo["rank_prefix"][R])
+    o = oracle.dispatch(x, idx, w, E, R, lo["token_slot"], True, N)
+    d_x, d_idx, d_w = U.to_dev_bf16(x), torch.from_numpy(idx).to(U.dev()), torch.from_numpy(w).to(U.dev())
+    lay, d = ep.ep_get_layout_and_dispatch(d_x, d_idx, d_w, E, R, dtype="fp8", recv_capacity=N)
+    for i in range(300):
+        if i % 50 == 25:
+            ep.ep_get_layout(d_idx, E, R, layout=lay)
+        ep.ep_get_layout_and_dispatch(d_x, d_idx, d_w, E, R, layout=lay, dtype="fp8", recv_capacity=N, out=d)
+    torch.cuda.synchronize()
+    assert lay.errors() == 0
+    U.assert_layout_equal(U.layout_np(lay), lo)
+    assert np.array_equal(U.bits(d.recv_x)[:N], o["recv_x"][:N])
+    assert np.array_equal(U.bits(d.recv_x_scales)[:N].view(np.uint32), o["recv_x_scales"][:N].view(np.uint32))
