@@ -176,3 +176,29 @@ def test_repeated_and_mixed_with_layout_kernel():
     U.assert_layout_equal(U.layout_np(lay), lo)
     assert np.array_equal(U.bits(d.recv_x)[:N], o["recv_x"][:N])
     assert np.array_equal(U.bits(d.recv_x_scales)[:N].view(np.uint32), o["recv_x_scales"][:N].view(np.uint32))
+
+
+def test_rows_written_just_before_the_call():
+    """x is rewritten by a device copy right before each call on the same
+    stream: the rows the dispatch loads before its wait for the layout must
+    be the new ones (the layout kernel waits for the copy before the
+    dispatch can start)."""
+    T, H, K, E, R = 8192, 2048, 8, 64, 8
+    idx, w, rng = _routing(T, K, E, 11, p_mask=0.0)
+    xs = [W.normal_bf16(rng, (T, H)) for _ in range(2)]
+    lo = oracle.get_layout(idx, E, R)
+    N = int(lo["rank_prefix"][R])
+    want = [oracle.dispatch(x, idx, w, E, R, lo["token_slot"], True, N) for x in xs]
+    d_xs = [U.to_dev_bf16(x) for x in xs]
+    d_x = torch.empty_like(d_xs[0])
+    d_idx, d_w = torch.from_numpy(idx).to(U.dev()), torch.from_numpy(w).to(U.dev())
+    lay, d = None, None
+    for i in range(12):
+        d_x.copy_(d_xs[i % 2])
+        lay, d = ep.ep_get_layout_and_dispatch(d_x, d_idx, d_w, E, R, layout=lay, dtype="fp8",
+                                               recv_capacity=N, out=d)
+        torch.cuda.synchronize()
+        assert np.array_equal(U.bits(d.recv_x)[:N], want[i % 2]["recv_x"][:N]), i
+        assert np.array_equal(U.bits(d.recv_x_scales)[:N].view(np.uint32),
+                              want[i % 2]["recv_x_scales"][:N].view(np.uint32)), i
+    assert lay.errors() == 0
