@@ -192,6 +192,14 @@ __device__ __forceinline__ void mul2_rn(float a, float b, float c, float &ac, fl
       : "f"(a), "f"(b), "f"(c));
 }
 
+// (a0 + y0, a1 + y1) as one packed f32x2 add, rounded to nearest even.
+__device__ __forceinline__ void add2_rn(float &a0, float &a1, float y0, float y1) {
+  asm("{\n\t.reg .b64 y, a;\n\tmov.b64 y, {%2, %3};\n\tmov.b64 a, {%0, %1};\n\t"
+      "add.rn.f32x2 a, a, y;\n\tmov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(y0), "f"(y1));
+}
+
 // ------------------------------------------------------------- grid barrier
 // For cooperative launches (all blocks co-resident).  The two words live in
 // caller-zeroed global memory; the last block out resets them, so the next

@@ -105,6 +105,16 @@ def assert_combine_close(g_bits: np.ndarray, o_bits: np.ndarray):
     assert np.all(g_bits[zero] == 0)
 
 
+def assert_combine_exact(g_bits: np.ndarray, o_bits: np.ndarray):
+    """The kernel sums in the oracle's order with the oracle's roundings (a
+    product, then a sum, each rounded to nearest even, ranks ascending), so
+    beyond the 2^-8 bar the results are expected to be identical; a fused
+    multiply-add anywhere shows up here first."""
+    assert_combine_close(g_bits, o_bits)
+    n = int(np.count_nonzero(g_bits != o_bits))
+    assert n == 0, f"combine: {n} elements differ from the oracle's (within 2^-8, but not bit-identical)"
+
+
 def subset_problem(token_ids: np.ndarray, token_slot: np.ndarray):
     """Restrict a routing's slots to some tokens: returns (local token_slot
     for those tokens with rows renumbered 0..n-1 in global order, the global

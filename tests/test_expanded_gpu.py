@@ -171,7 +171,7 @@ def test_expanded_combine(case):
     torch.cuda.synchronize()
     assert lay.errors() == 0 and err == 0
     g = U.bits(out)
-    U.assert_combine_close(g, o)
+    U.assert_combine_exact(g, o)
     assert np.array_equal(g, o)
 
 

@@ -106,7 +106,7 @@ def test_combine_bias(R, E, biases, weighted):
     torch.cuda.synchronize()
     assert lay.errors() == 0
     g = U.bits(out)
-    U.assert_combine_close(g, o)
+    U.assert_combine_exact(g, o)
     assert np.array_equal(g, o)
     if b0 is not None and b1 is None:
         assert np.array_equal(g[:20], b0[:20])

@@ -59,7 +59,7 @@ def test_workload_parity(name, weighted):
     g, lay_o, d_o, c_o, N = _full_case(cfg, weighted=weighted)
     U.assert_layout_equal(g["layout"], lay_o)
     U.assert_dispatch_equal(g, d_o, N, cfg.fp8)
-    U.assert_combine_close(g["combined"], c_o)
+    U.assert_combine_exact(g["combined"], c_o)
     assert np.array_equal(g["combined"], c_o), "combine is not bit-exact"
 
 
@@ -90,7 +90,7 @@ def test_large_workload_sampled():
     d_o["recv_src_idx"] = toks[d_o["recv_src_idx"]]
     U.assert_dispatch_equal(sub, d_o, len(glob), True)
     c_o, _ = oracle.combine(y[glob], local, inp["topk_idx"][toks], inp["topk_weights"][toks], E)
-    U.assert_combine_close(g["combined"][toks], c_o)
+    U.assert_combine_exact(g["combined"][toks], c_o)
     assert np.array_equal(g["combined"][toks], c_o)
 
 
@@ -152,7 +152,7 @@ def test_edge_parity(case):
     g, lay_o, d_o, c_o, N = _custom(T, H, K, E, R, fp8, **kw)
     U.assert_layout_equal(g["layout"], lay_o)
     U.assert_dispatch_equal(g, d_o, N, fp8)
-    U.assert_combine_close(g["combined"], c_o)
+    U.assert_combine_exact(g["combined"], c_o)
     assert np.array_equal(g["combined"], c_o)
 
 
