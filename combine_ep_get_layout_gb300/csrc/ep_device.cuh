@@ -73,6 +73,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
 // ------------------------------------------------------- bulk (TMA 1D) copy
 // Sizes and both addresses must be multiples of 16 bytes.
 
+// A hint that `bytes` of global memory at src (both multiples of 16) will be
+// read soon: the lines are brought into L2.  No value is returned, so it is
+// safe on memory another kernel may still be writing (L2 is where its writes
+// land).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src_gmem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, uint32_t bytes,
                                           uint64_t *bar) {
   asm volatile(

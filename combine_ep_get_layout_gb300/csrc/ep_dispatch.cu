@@ -34,6 +34,7 @@ constexpr size_t kSmemBudget = 80 * 1024;  // per CTA: aims at >= 2-3 CTAs per S
 constexpr int kWsStages = 2;                 // bf16 row stages of the fp8 kernel
 constexpr size_t kWsSmemBudget = 64 * 1024;
 constexpr bool kFp8WarpSpecialised = true;
+constexpr bool kWsWarmL2 = true;  // fp8 kernel: L2 hints before the grid-dependency wait
 
 struct DispatchParams {
   const uint16_t *x;
@@ -471,7 +472,17 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
   // while the layout is still running; the loader waits before its first
   // ticket, the storer before it reads the layout.  The casters touch no
   // global memory.
-  if (p.early == 0) griddep_wait();
+  if (p.early == 0) {
+    // Before the wait, only hints: the row of token blockIdx.x (the first
+    // tickets go to tokens 0 .. gridDim.x - 1 in some order) and its layout
+    // row are brought into L2, no value is read.
+    if (kWsWarmL2 && tid == 0 && (int)blockIdx.x < p.T) {
+      bulk_prefetch_l2(p.x + (size_t)blockIdx.x * p.H, p.row_in_bytes);
+      prefetch_l2(p.token_slot + (size_t)blockIdx.x * p.D);
+      prefetch_l2(p.topk_idx + (size_t)blockIdx.x * p.K);
+    }
+    griddep_wait();
+  }
   griddep_launch_dependents();
 
   int issued = 0;        // loader lane 0: token indices drawn (loads and the end)
