@@ -254,7 +254,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
 // the per-token metadata or on the reduction.
 
 constexpr int kWsMaxRanks = 8;
-constexpr bool kWarmL2 = true;  // warm L2 with the first tokens before the grid-dependency wait
+// L2 warm-up before the grid-dependency wait: tokens per block, leading
+// chunks of each of their rows
+constexpr int kWarmTokens = 2;
+constexpr int kWarmChunks = 1;
 constexpr int kChunk = 2048;                   // elements per unit
 constexpr int kChunkBytes = kChunk * 2;
 constexpr int kReducers = 8;                   // warps
@@ -301,20 +304,25 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
     fence_barrier_init();
   }
   __syncthreads();
-  if (kWarmL2 && warp == 0 && (int)blockIdx.x < p.T) {
+  if (kWarmTokens > 0 && warp == 0) {
     // Before the wait for the kernel ahead, nothing is read for its value:
-    // the first tokens' metadata and the first chunk of their rows are only
-    // brought into L2 (block b warms token b; the first tickets go to
-    // tokens 0 .. gridDim.x - 1 in some order).  The slots read here may be
-    // stale; they serve as addresses only, checked against the capacity.
-    const int t = blockIdx.x;
-    const int slot = lane < p.D ? __ldcg(p.token_slot + (size_t)t * p.D + lane) : -1;
-    if (lane == 0) {
-      prefetch_l2(p.token_slot + (size_t)t * p.D);
-      if (p.topk_idx != nullptr) prefetch_l2(p.topk_idx + (size_t)t * p.K);
-      if (p.topk_weights != nullptr) prefetch_l2(p.topk_weights + (size_t)t * p.K);
+    // the first tokens' metadata and the first chunks of their rows are only
+    // brought into L2.  The first tickets go to tokens 0, 1, ... in some
+    // order, so block b warms tokens b, b + gridDim.x, ...  The slots read
+    // here may be stale; they serve as addresses only, checked against the
+    // capacity.
+    for (int k = 0; k < kWarmTokens; ++k) {
+      const int t = (int)blockIdx.x + k * (int)gridDim.x;
+      if (t >= p.T) break;
+      const int slot = lane < p.D ? __ldcg(p.token_slot + (size_t)t * p.D + lane) : -1;
+      if (lane == 0) {
+        prefetch_l2(p.token_slot + (size_t)t * p.D);
+        if (p.topk_idx != nullptr) prefetch_l2(p.topk_idx + (size_t)t * p.K);
+        if (p.topk_weights != nullptr) prefetch_l2(p.topk_weights + (size_t)t * p.K);
+      }
+      if (slot >= 0 && slot < p.cap)
+        bulk_prefetch_l2(p.y + (size_t)slot * p.H, (uint32_t)min(kWarmChunks * kChunk, p.H) * 2u);
     }
-    if (slot >= 0 && slot < p.cap) bulk_prefetch_l2(p.y + (size_t)slot * p.H, (uint32_t)min(kChunk, p.H) * 2u);
   }
   griddep_wait();
   griddep_launch_dependents();
