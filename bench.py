@@ -67,11 +67,12 @@ KERNEL_SOURCES = {
     "combine": ["ep_combine.cu", "ep_device.cuh"],
 }
 def kernel_symbol(kernel: str, cfg: W.EPConfig) -> str:
-    """The library kernel that runs each call for this workload (the library
-    picks the warp-specialised fp8 dispatch, the ring kernel for bf16, and
-    the warp-specialised combine for up to 8 ranks)."""
+    """The library kernel(s) that run each call for this workload (the
+    layout is two kernels; the library picks the warp-specialised fp8
+    dispatch, the ring kernel for bf16, and the warp-specialised combine for
+    up to 8 ranks)."""
     if kernel == "layout":
-        return "layout_kernel"
+        return "layout_count_kernel+layout_slot_kernel"
     if kernel == "dispatch":
         return "dispatch_ws_kernel" if cfg.fp8 else "dispatch_ring_kernel"
     return "combine_ws_kernel" if cfg.num_ranks <= 8 else "combine_kernel"
@@ -355,7 +356,7 @@ def run_ours(args, rank, world, local):
         barrier(world)
     ms_per_step = ev0.elapsed_time(ev1) / args.steps
     ms_per_step = max_over_ranks(ms_per_step, world)
-    launches = 3 * args.steps
+    launches = 4 * args.steps  # layout (count, slots), dispatch, combine
 
     # (2) the same steps with an event between kernels: per-kernel durations.
     k_steps = min(args.steps, 500)

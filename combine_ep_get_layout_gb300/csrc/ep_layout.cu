@@ -1,24 +1,23 @@
-// Layout kernel: the count phase and the count exchange of TileScale PR #68
-// ("[Example] EP v2 intranode dispatch/combine", README section "Design"),
-// on one GPU where the expert-parallel ranks are logical partitions of the
-// expert set.
+// Layout kernels: the count phase and the count exchange of TileScale PR
+// #68 ("[Example] EP v2 intranode dispatch/combine", README section
+// "Design"), on one GPU where the expert-parallel ranks are logical
+// partitions of the expert set.  Two ordinary launches, the kernel boundary
+// standing in for the pages' count exchange between ranks:
 //
-//   phase 1  each block owns a contiguous range of tokens.  Per token it
-//            validates the K expert ids, counts them in a shared-memory
-//            histogram (shared atomics) and ORs rank bits into a 64-bit mask,
-//            so a token is in a rank once however many of its experts live
-//            there (the pages' per-(token, destination) dedup).  Warp ballots
-//            turn the masks into per-rank block totals.
-//   exchange the block totals go to global memory; a bounded grid barrier
-//            (cooperative launch: all blocks are co-resident) stands in for
-//            the pages' count exchange between ranks.
-//   phase 2  every block scans the totals of the blocks before it, which
-//            gives rank_prefix (the pages' send_base[d]) plus this block's
-//            first slot in each rank; warp ballots and a shared scan over
-//            warps then give each (token, rank) its slot in ascending token
+//   layout_count_kernel  each block owns a contiguous range of tokens.  Per
+//            token it validates the K expert ids and ORs rank bits into a
+//            64-bit mask, so a token is in a rank once however many of its
+//            experts live there (the pages' per-(token, destination) dedup).
+//            Warp ballots turn the masks into per-rank block totals, written
+//            to the workspace.
+//   layout_slot_kernel   every block re-reads its tokens' ids (from L2),
+//            rebuilds the masks and counts the ids in a shared-memory
+//            histogram (shared atomics), scans the block totals of all
+//            blocks (rank_prefix, the pages' send_base[d], plus this block's
+//            first slot in each rank), then warp ballots and a shared scan
+//            over warps give each (token, rank) its slot in ascending token
 //            order (a stable scatter).
 #include <algorithm>
-#include <mutex>
 
 #include "ep_device.cuh"
 
@@ -27,105 +26,117 @@ namespace {
 
 constexpr int kLayoutThreads = 256;  // one token per thread per chunk
 constexpr int kLayoutWarps = kLayoutThreads / kWarpSize;
-constexpr size_t kPartialOffset = 256;  // bytes: barrier words come first
+constexpr size_t kPartialOffset = 256;  // bytes of the workspace before the block totals (unused)
+constexpr int kMaxLayoutBlocks = 2048;  // more tokens per block beyond this
 
 struct LayoutParams {
   const int64_t *topk_idx;
   int num_tokens, num_topk, num_experts, num_ranks, experts_per_rank;
   int tokens_per_block;
   ep_layout_t out;
-  GridBarrierWords *bar;
   int32_t *partial;  // [gridDim.x * R] per-block, per-rank token counts
 };
 
-size_t layout_smem_bytes(int tokens_per_block, int E, int R) {
-  // masks[tpb] u64, hist[E], blk_cnt[R], warp_off[W*R], chunk_tot[R],
-  // tot[R], before[R], base[R+1], run[R], flags[2], scan_all[T], scan_before[T]
-  size_t ints = (size_t)E + R + (size_t)kLayoutWarps * R + R + R + R + (R + 1) + R + 3 + 2 * kLayoutThreads;
-  return (size_t)tokens_per_block * sizeof(uint64_t) + ints * sizeof(int32_t);
+// The rank mask of token t (ids of row `ids`), the count of each valid id in
+// `hist` (shared; null to skip) and `bad` for an id outside [-1, E).
+template <int KMAX>
+__device__ __forceinline__ uint64_t rank_mask(const int64_t (&ids)[KMAX], int K, int E, int epr, int *hist,
+                                              bool &bad) {
+  uint64_t mask = 0;
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) {
+    const int64_t e = ids[k];
+    if (k >= K || e == -1) continue;
+    if (e < 0 || e >= E) {
+      bad = true;
+      continue;
+    }
+    const int ei = static_cast<int>(e);
+    if (hist != nullptr) atomicAdd(&hist[ei], 1);
+    mask |= 1ull << (ei / epr);
+  }
+  return mask;
 }
 
-// KMAX bounds the unrolled index loads: all K ids of a token are requested
-// before the first is used.
 template <int KMAX>
-__global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutParams p) {
+__device__ __forceinline__ void load_ids(const LayoutParams &p, int t, int end, int64_t (&ids)[KMAX]) {
+  const int64_t *row = p.topk_idx + (size_t)t * p.num_topk;
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) ids[k] = (t < end && k < p.num_topk) ? __ldg(row + k) : -1;
+}
+
+template <int KMAX>
+__global__ void __launch_bounds__(kLayoutThreads) layout_count_kernel(LayoutParams p) {
+  __shared__ int blk_cnt[EP_MAX_RANKS];
+  const int tid = threadIdx.x;
+  const int lane = tid & (kWarpSize - 1);
+  const int b = blockIdx.x;
+  const int R = p.num_ranks, E = p.num_experts;
+  for (int r = tid; r < R; r += kLayoutThreads) blk_cnt[r] = 0;
+  __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();
+  if (b == 0) {  // the slot kernel adds into them, after this kernel
+    for (int i = tid; i < E; i += kLayoutThreads) p.out.num_tokens_per_expert[i] = 0;
+    if (tid == 0) *p.out.error_word = 0u;
+    if (tid < EP_WORK_COUNTER_WORDS && p.out.work_counters != nullptr) p.out.work_counters[tid] = 0u;
+  }
+  const int begin = min(b * p.tokens_per_block, p.num_tokens);
+  const int end = min(begin + p.tokens_per_block, p.num_tokens);
+  bool bad = false;
+  for (int c0 = begin; c0 < end; c0 += kLayoutThreads) {
+    int64_t ids[KMAX];
+    load_ids(p, c0 + tid, end, ids);
+    const uint64_t mask = rank_mask(ids, p.num_topk, E, p.experts_per_rank, nullptr, bad);
+    for (int r = 0; r < R; ++r) {
+      const uint32_t bal = __ballot_sync(0xffffffffu, (mask >> r) & 1ull);
+      if (lane == 0 && bal != 0u) atomicAdd(&blk_cnt[r], __popc(bal));
+    }
+  }
+  __syncthreads();
+  for (int r = tid; r < R; r += kLayoutThreads) p.partial[(size_t)b * R + r] = blk_cnt[r];
+}
+
+size_t slot_smem_bytes(int E, int R) {
+  // hist[E], warp_off[W*R], chunk_tot[R], tot[R], before[R], base[R+1], run[R],
+  // flags[1], scan_all[T], scan_before[T]
+  return ((size_t)E + (size_t)kLayoutWarps * R + 4 * (size_t)R + (R + 1) + 1 + 2 * kLayoutThreads) * sizeof(int32_t);
+}
+
+template <int KMAX>
+__global__ void __launch_bounds__(kLayoutThreads) layout_slot_kernel(LayoutParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x;
   const int lane = tid & (kWarpSize - 1);
   const int warp = tid / kWarpSize;
   const int G = gridDim.x;
   const int b = blockIdx.x;
-  const int R = p.num_ranks, E = p.num_experts, K = p.num_topk;
-
-  uint64_t *masks = reinterpret_cast<uint64_t *>(smem);
-  int *hist = reinterpret_cast<int *>(masks + p.tokens_per_block);
-  int *blk_cnt = hist + E;
-  int *warp_off = blk_cnt + R;  // [kLayoutWarps][R]
+  const int R = p.num_ranks, E = p.num_experts;
+  int *hist = reinterpret_cast<int *>(smem);
+  int *warp_off = hist + E;  // [kLayoutWarps][R]
   int *chunk_tot = warp_off + kLayoutWarps * R;
   int *tot = chunk_tot + R;
   int *before = tot + R;
   int *base = before + R;  // [R + 1]
   int *run = base + R + 1;
-  int *flags = run + R;  // [0] bad index seen, [1] barrier timed out, [2] barrier scratch
-  int *scan_all = flags + 3;                  // [kLayoutThreads]
+  int *flags = run + R;  // [0] bad index seen
+  int *scan_all = flags + 1;                     // [kLayoutThreads]
   int *scan_before = scan_all + kLayoutThreads;  // [kLayoutThreads]
-
   for (int i = tid; i < E; i += kLayoutThreads) hist[i] = 0;
-  for (int i = tid; i < R; i += kLayoutThreads) blk_cnt[i] = 0;
-  if (tid < 2) flags[tid] = 0;
-  griddep_wait();
-  griddep_launch_dependents();
-  if (b == 0) {
-    // Cleared before the barrier; every block adds into them after it.
-    for (int i = tid; i < E; i += kLayoutThreads) p.out.num_tokens_per_expert[i] = 0;
-    if (tid == 0) *p.out.error_word = 0u;
-    if (tid < EP_WORK_COUNTER_WORDS && p.out.work_counters != nullptr) p.out.work_counters[tid] = 0u;
-  }
+  if (tid == 0) flags[0] = 0;
   __syncthreads();
+  // The kernel after this one waits for it to complete (and so for the count
+  // kernel too) before it reads the layout: it may start early.
+  griddep_launch_dependents();
+  griddep_wait();
 
   const int begin = min(b * p.tokens_per_block, p.num_tokens);
   const int end = min(begin + p.tokens_per_block, p.num_tokens);
+  int64_t ids[KMAX];
+  load_ids(p, begin + tid, end, ids);  // in flight during the scan
 
-  // ---- phase 1: count
-  bool bad = false;
-  for (int c0 = begin; c0 < end; c0 += kLayoutThreads) {
-    const int t = c0 + tid;
-    uint64_t mask = 0;
-    if (t < end) {
-      const int64_t *row = p.topk_idx + (size_t)t * K;
-      int64_t ids[KMAX];
-#pragma unroll
-      for (int k = 0; k < KMAX; ++k) ids[k] = k < K ? __ldg(row + k) : -1;
-#pragma unroll
-      for (int k = 0; k < KMAX; ++k) {
-        const int64_t e = ids[k];
-        if (e == -1) continue;
-        if (e < 0 || e >= E) {
-          bad = true;
-          continue;
-        }
-        const int ei = static_cast<int>(e);
-        atomicAdd(&hist[ei], 1);
-        mask |= 1ull << (ei / p.experts_per_rank);
-      }
-      masks[t - begin] = mask;
-    }
-    for (int r = 0; r < R; ++r) {
-      const uint32_t bal = __ballot_sync(0xffffffffu, (mask >> r) & 1ull);
-      if (lane == 0 && bal != 0u) atomicAdd(&blk_cnt[r], __popc(bal));
-    }
-  }
-  if (bad) flags[0] = 1;
-  __syncthreads();
-  for (int r = tid; r < R; r += kLayoutThreads) p.partial[(size_t)b * R + r] = blk_cnt[r];
-
-  // ---- exchange: bounded grid barrier (all blocks co-resident)
-  __threadfence();
-  if (!grid_barrier(p.bar, &flags[2]) && tid == 0) flags[1] = 1;
-
-  // ---- phase 2: bases (exclusive scan over ranks and over earlier blocks);
-  // the block totals are summed by kLayoutThreads / R threads per rank
-  const int per_rank = kLayoutThreads / R;  // >= 2 since R <= 64
+  // bases: exclusive scan over ranks and over earlier blocks
+  const int per_rank = kLayoutThreads / R;  // >= 4 since R <= 64
   if (tid < per_rank * R) {
     const int r = tid % R;
     int all = 0, earlier = 0;
@@ -163,21 +174,17 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutParams p) 
       if (r < R) p.out.num_tokens_per_rank[r] = tot[r];
     }
   }
-  for (int e = tid; e < E; e += kLayoutThreads)
-    if (hist[e] != 0) atomicAdd(&p.out.num_tokens_per_expert[e], hist[e]);
-  if (tid == 0) {
-    const uint32_t bits = (flags[0] ? EP_ERRBIT_BAD_INDEX : 0u) | (flags[1] ? EP_ERRBIT_TIMEOUT : 0u);
-    if (bits) atomicOr(p.out.error_word, bits);
-  }
   for (int r = tid; r < R; r += kLayoutThreads) run[r] = base[r] + before[r];
   __syncthreads();
 
-  // ---- phase 2: slots, in ascending token order within each rank
+  // slots, in ascending token order within each rank
   const uint32_t lanes_below = (1u << lane) - 1u;
   const bool vec4 = (R % 4) == 0;
+  bool bad = false;
   for (int c0 = begin; c0 < end; c0 += kLayoutThreads) {
     const int t = c0 + tid;
-    const uint64_t mask = (t < end) ? masks[t - begin] : 0ull;
+    if (c0 != begin) load_ids(p, t, end, ids);
+    const uint64_t mask = rank_mask(ids, p.num_topk, E, p.experts_per_rank, hist, bad);
     for (int r = 0; r < R; ++r) {
       const uint32_t bal = __ballot_sync(0xffffffffu, (mask >> r) & 1ull);
       if (lane == 0) warp_off[warp * R + r] = __popc(bal);
@@ -196,27 +203,27 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutParams p) 
     int32_t *slot_row = p.out.token_slot + (size_t)t * R;
     uint8_t *in_row = p.out.is_token_in_rank + (size_t)t * R;
     for (int r0 = 0; r0 < R; r0 += 4) {
-      int s[4];
+      int sl[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int r = r0 + q;
-        s[q] = -1;
+        sl[q] = -1;
         if (r < R) {  // uniform across the warp
           const bool in = (mask >> r) & 1ull;
           const uint32_t bal = __ballot_sync(0xffffffffu, in);
-          if (in) s[q] = run[r] + warp_off[warp * R + r] + __popc(bal & lanes_below);
+          if (in) sl[q] = run[r] + warp_off[warp * R + r] + __popc(bal & lanes_below);
         }
       }
       if (t < end) {
         if (vec4) {
-          *reinterpret_cast<int4 *>(slot_row + r0) = make_int4(s[0], s[1], s[2], s[3]);
-          const uint32_t bytes = (s[0] >= 0 ? 1u : 0u) | (s[1] >= 0 ? 1u << 8 : 0u) |
-                                 (s[2] >= 0 ? 1u << 16 : 0u) | (s[3] >= 0 ? 1u << 24 : 0u);
+          *reinterpret_cast<int4 *>(slot_row + r0) = make_int4(sl[0], sl[1], sl[2], sl[3]);
+          const uint32_t bytes = (sl[0] >= 0 ? 1u : 0u) | (sl[1] >= 0 ? 1u << 8 : 0u) |
+                                 (sl[2] >= 0 ? 1u << 16 : 0u) | (sl[3] >= 0 ? 1u << 24 : 0u);
           *reinterpret_cast<uint32_t *>(in_row + r0) = bytes;
         } else {
           for (int q = 0; q < 4 && r0 + q < R; ++q) {
-            slot_row[r0 + q] = s[q];
-            in_row[r0 + q] = s[q] >= 0 ? 1 : 0;
+            slot_row[r0 + q] = sl[q];
+            in_row[r0 + q] = sl[q] >= 0 ? 1 : 0;
           }
         }
       }
@@ -225,9 +232,11 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutParams p) 
     for (int r = tid; r < R; r += kLayoutThreads) run[r] += chunk_tot[r];
     __syncthreads();
   }
-
-  // ---- exit: the last block out resets the barrier words for the next call
-  grid_barrier_exit(p.bar);
+  if (bad) flags[0] = 1;
+  __syncthreads();
+  for (int e = tid; e < E; e += kLayoutThreads)
+    if (hist[e] != 0) atomicAdd(&p.out.num_tokens_per_expert[e], hist[e]);
+  if (tid == 0 && flags[0]) atomicOr(p.out.error_word, EP_ERRBIT_BAD_INDEX);
 }
 
 int max_layout_blocks(int num_tokens) {
@@ -245,45 +254,10 @@ size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks) {
 ep_status_t launch_layout(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
                           int num_ranks, const ep_layout_t &layout, void *workspace,
                           cudaStream_t stream) {
-  const DeviceInfo *di = current_device_info();
-  if (di == nullptr) return EP_ERR_CUDA;
-
-  const auto kernel = num_topk <= 8 ? layout_kernel<8> : layout_kernel<EP_MAX_TOPK>;
-  static std::mutex mu;
-  static bool configured[64] = {};
-  {
-    std::lock_guard<std::mutex> g(mu);
-    if (di->device < 64 && !configured[di->device]) {
-      for (auto k : {layout_kernel<8>, layout_kernel<EP_MAX_TOPK>}) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)di->max_smem_per_block_optin);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(layout_kernel)");
-      }
-      configured[di->device] = true;
-    }
-  }
-
-  // Grid: one block per 256 tokens, capped at what can be co-resident.
-  int grid = max_layout_blocks(num_tokens);
-  size_t smem = 0;
-  for (int iter = 0;; ++iter) {
-    const int tpb = (num_tokens + grid - 1) / grid;
-    smem = layout_smem_bytes(tpb, num_experts, num_ranks);
-    if (smem > di->max_smem_per_block_optin)
-      return fail(EP_ERR_UNSUPPORTED,
-                  "ep_get_layout: %d tokens need %zu bytes of shared memory per block (max %zu)",
-                  num_tokens, smem, di->max_smem_per_block_optin);
-    int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kLayoutThreads, smem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(layout)");
-    const int cap = per_sm * di->num_sms;
-    if (cap <= 0) return fail(EP_ERR_UNSUPPORTED, "ep_get_layout: layout kernel cannot be resident");
-    if (grid <= cap) break;
-    if (iter > 8) return fail(EP_ERR_UNSUPPORTED, "ep_get_layout: no co-resident grid found");
-    grid = cap;
-  }
-
+  // One block per 256 tokens, at most kMaxLayoutBlocks (then more tokens per
+  // block): every slot block scans all blocks' totals.
   LayoutParams p;
+  const int grid = std::min(max_layout_blocks(num_tokens), kMaxLayoutBlocks);
   p.topk_idx = topk_idx;
   p.num_tokens = num_tokens;
   p.num_topk = num_topk;
@@ -292,11 +266,15 @@ ep_status_t launch_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
   p.experts_per_rank = num_experts / num_ranks;
   p.tokens_per_block = (num_tokens + grid - 1) / grid;
   p.out = layout;
-  p.bar = static_cast<GridBarrierWords *>(workspace);
   p.partial = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(workspace) + kPartialOffset);
-
-  cudaError_t e = launch_kernel(kernel, grid, kLayoutThreads, smem, stream, true, p);
-  if (e != cudaSuccess) return cuda_fail(e, "launch layout_kernel");
+  const bool wide = num_topk > 8;
+  cudaError_t e = wide ? launch_kernel(layout_count_kernel<EP_MAX_TOPK>, grid, kLayoutThreads, 0, stream, false, p)
+                       : launch_kernel(layout_count_kernel<8>, grid, kLayoutThreads, 0, stream, false, p);
+  if (e != cudaSuccess) return cuda_fail(e, "launch layout_count_kernel");
+  const size_t smem = slot_smem_bytes(num_experts, num_ranks);
+  e = wide ? launch_kernel(layout_slot_kernel<EP_MAX_TOPK>, grid, kLayoutThreads, smem, stream, false, p)
+           : launch_kernel(layout_slot_kernel<8>, grid, kLayoutThreads, smem, stream, false, p);
+  if (e != cudaSuccess) return cuda_fail(e, "launch layout_slot_kernel");
   return EP_OK;
 }
 

@@ -14,7 +14,7 @@
 namespace ep {
 namespace {
 
-// Scratch of the layout kernel (barrier words, per-block rank totals).
+// Scratch of the layout kernels (the per-block rank totals they exchange).
 // Zero at module load; every GPU that loads the library holds it until exit.
 __device__ __align__(256) unsigned char g_layout_scratch[EP_NOALLOC_SCRATCH_BYTES];
 

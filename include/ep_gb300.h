@@ -123,11 +123,11 @@ typedef struct {
 } ep_layout_t;
 
 /*
- * Bytes of device workspace ep_get_layout needs for these sizes.  The
- * workspace must be zero-filled once when it is allocated; every call
- * leaves it zeroed again on exit, so it can be reused by later calls with
- * any sizes up to the ones it was sized for.  Calls sharing one workspace
- * must be ordered (the same stream, or events).
+ * Bytes of device workspace ep_get_layout needs for these sizes: the
+ * per-block, per-rank token totals its two kernels exchange.  It needs no
+ * initialisation (each call writes every total it reads) and can be reused
+ * by later calls with any sizes up to the ones it was sized for.  Calls
+ * sharing one workspace must be ordered (the same stream, or events).
  */
 size_t ep_layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
 
@@ -135,18 +135,20 @@ size_t ep_layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks)
  * Layout: the count phase and the count exchange of TileScale PR #68
  * (README section "Design"; commit message on do_expand: "phase 1 tallies
  * per destination, phase 2 turns tallies into a base, phase 3 adds a
- * locally-claimed slot"), on one GPU.  One cooperative kernel: each block
- * counts its tokens' experts (shared-memory atomics) and ranks (warp
- * ballots, one bit per (token, rank) however many experts map there),
- * publishes per-rank block totals, waits at a bounded grid barrier, then
- * derives each rank's base by an exclusive scan and writes token_slot.
+ * locally-claimed slot"), on one GPU.  Two kernels, the boundary between
+ * them standing in for the count exchange: the first counts each block's
+ * tokens per rank (warp ballots, one bit per (token, rank) however many
+ * experts map there) and publishes per-rank block totals; the second
+ * re-reads the ids, counts the experts (shared-memory atomics), derives
+ * each rank's base and the block's first slot in it by an exclusive scan of
+ * the totals, and writes token_slot.
  *
  *   topk_idx  [T*K] int64, device.
  *   T >= 0 (T == 0 writes zero counts), 1 <= K <= EP_MAX_TOPK,
  *   1 <= R <= EP_MAX_RANKS, R <= E <= EP_MAX_EXPERTS, E % R == 0.
  *   layout    every member non-null (token_slot 16-byte aligned).
- *   workspace >= ep_layout_workspace_bytes(T, E, R) bytes, zero-filled at
- *             allocation (see above), 16-byte aligned.
+ *   workspace >= ep_layout_workspace_bytes(T, E, R) bytes, 16-byte
+ *             aligned (see above).
  */
 ep_status_t ep_get_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
                           int num_experts, int num_ranks,
@@ -163,8 +165,8 @@ ep_status_t ep_get_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
  * that owns all device memory and forbids new allocations once it is built),
  * or a latency-critical serving loop where a cudaMalloc or cudaFree could
  * synchronise the device and stall every other stream.  This entry point
- * takes no workspace: its scratch (the layout kernel's barrier words and
- * per-block rank totals) is a file-scope static device array of
+ * takes no workspace: its scratch (the per-block rank totals the layout
+ * kernels exchange) is a file-scope static device array of
  * EP_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
  * the library holds until the process exits.  It calls no allocating
  * routine.  The caller still passes topk_idx and the layout outputs.
