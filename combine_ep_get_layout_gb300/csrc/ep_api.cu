@@ -236,7 +236,19 @@ ep_status_t ep_get_layout_and_dispatch(const ep_dispatch_args_t *args, void *wor
   if (workspace_bytes < need)
     return fail(EP_ERR_INVALID_ARG, "%s: workspace_bytes=%zu < %zu needed", fn, workspace_bytes, need);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  EP_CHECK(launch_layout(args->topk_idx, a.num_tokens, a.num_topk, a.num_experts, a.num_ranks, *layout, workspace, s));
+  if (a.fp8 && a.num_tokens > 0 && a.num_tokens <= local_layout_max_tokens()) {
+    // One layout launch; the dispatch finishes the slots (adds each block's
+    // base, writes them back) and counts the experts as it moves the rows.
+    const int32_t *local_base = nullptr;
+    EP_CHECK(launch_layout_local(args->topk_idx, a.num_tokens, a.num_topk, a.num_experts, a.num_ranks, *layout,
+                                 workspace, s, &local_base));
+    a.local_base = local_base;
+    a.token_slot_out = layout->token_slot;
+    a.num_tokens_per_expert = layout->num_tokens_per_expert;
+  } else {
+    EP_CHECK(launch_layout(args->topk_idx, a.num_tokens, a.num_topk, a.num_experts, a.num_ranks, *layout, workspace,
+                           s));
+  }
   // The kernel ahead of the dispatch is the layout, which writes nothing the
   // dispatch reads before its wait; so its first rows load and cast early.
   a.early_rows = kEarlyRows;

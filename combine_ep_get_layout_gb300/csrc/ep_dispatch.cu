@@ -63,6 +63,11 @@ struct DispatchParams {
   uint32_t scale_stride;   // fp8 scales of one row, groups*4 rounded up to 16
   TokenSource tokens;      // the order in which blocks take tokens
   int early;               // fp8 kernel: rows loaded and cast before the wait for the previous kernel
+  // fp8 kernel after the local layout: token_slot holds block-relative slots;
+  // slot = relative + local_base[(t / 256) * R + r], written to token_slot_out
+  const int32_t *local_base;
+  int32_t *token_slot_out;
+  int32_t *num_tokens_per_expert;
 };
 
 // Token ids travel from the loading thread to the other roles of a block
@@ -537,8 +542,25 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
       const int64_t e = lane < p.K ? __ldg(p.topk_idx + (size_t)t * p.K + lane) : -1;
       const float w = (lane < p.K && p.recv_topk_weights != nullptr)
                           ? __ldg(p.topk_weights + (size_t)t * p.K + lane) : 0.0f;
-      if (!layout_agrees(p, e, slot_lo, slot_hi, lane) && lane == 0)
+      // local layout: the block's bases, loaded alongside the slots
+      const int32_t *blk = p.local_base + (size_t)(t / kLocalTokensPerBlock) * p.R;
+      const int base_lo = (p.local_base != nullptr && lane < p.D) ? __ldg(blk + lane) : 0;
+      const int base_hi = (p.local_base != nullptr && lane + kWarpSize < p.D) ? __ldg(blk + lane + kWarpSize) : 0;
+      if (p.local_base != nullptr) {
+        // finish the layout of token t: absolute slots, written back; its
+        // experts counted; ids outside [-1, E) flagged
+        if (slot_lo >= 0) slot_lo += base_lo;
+        if (slot_hi >= 0) slot_hi += base_hi;
+        int32_t *orow = p.token_slot_out + (size_t)t * p.D;
+        if (lane < p.D) orow[lane] = slot_lo;
+        if (lane + kWarpSize < p.D) orow[lane + kWarpSize] = slot_hi;
+        const bool valid = e >= 0 && e < p.E;
+        if (valid) atomicAdd(p.num_tokens_per_expert + e, 1);
+        if (__any_sync(0xffffffffu, !valid && e != -1 && lane < p.K) && lane == 0)
+          set_error(p.error_word, EP_ERRBIT_BAD_INDEX);
+      } else if (!layout_agrees(p, e, slot_lo, slot_hi, lane) && lane == 0) {
         set_error(p.error_word, EP_ERRBIT_STALE_LAYOUT);
+      }
       if (slot_lo >= p.cap) {
         set_error(p.error_word, EP_ERRBIT_CAPACITY);
         slot_lo = -1;
@@ -867,11 +889,15 @@ ep_status_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream) {
   p.tokens.done = a.work_counters != nullptr ? a.work_counters + 1 : nullptr;
   p.tokens.T = a.num_tokens;
   p.early = a.early_rows;
+  p.local_base = a.local_base;
+  p.token_slot_out = a.token_slot_out;
+  p.num_tokens_per_expert = a.num_tokens_per_expert;
   ep_status_t st = EP_OK;
   if (a.num_tokens > 0) {
     // packed rows are only built by the warp-specialised kernel
     if (a.fp8)
-      st = (kFp8WarpSpecialised || p.packed) ? launch_ws(p, *di, stream) : launch_ring<true>(p, *di, stream);
+      st = (kFp8WarpSpecialised || p.packed || p.local_base != nullptr) ? launch_ws(p, *di, stream)
+                                                                         : launch_ring<true>(p, *di, stream);
     else
       st = launch_ring<false>(p, *di, stream);
   }

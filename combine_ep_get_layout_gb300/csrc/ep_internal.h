@@ -38,6 +38,19 @@ ep_status_t launch_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
                           int num_ranks, const ep_layout_t &layout, void *workspace,
                           cudaStream_t stream);
 
+// The first half of a layout whose slots the fp8 dispatch finishes
+// (ep_get_layout_and_dispatch): one launch writes is_token_in_rank, each
+// (token, rank)'s slot relative to its 256-token block into token_slot, and
+// in the workspace each block's first slot in each rank (*local_base, [G*R],
+// G = ceil(T / 256)); rank_prefix and num_tokens_per_rank are final.  The
+// dispatch adds the block's base to each slot, writes it back and counts
+// num_tokens_per_expert and bad ids.  Applies to 0 < T <= local_layout_max_tokens().
+int local_layout_max_tokens();
+constexpr int kLocalTokensPerBlock = 256;
+ep_status_t launch_layout_local(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
+                                int num_ranks, const ep_layout_t &layout, void *workspace, cudaStream_t stream,
+                                const int32_t **local_base);
+
 // ---- expanded layout (ep_layout_expanded.cu)
 size_t expanded_layout_workspace_bytes(int num_tokens, int num_experts);
 ep_status_t launch_layout_expanded(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
@@ -78,6 +91,12 @@ struct DispatchArgs {
   // fp8 rows: tokens per block loaded and cast before the wait for the
   // previous kernel on the stream; only when that kernel writes none of x
   int early_rows = 0;
+  // after launch_layout_local (fp8 rows only): token_slot holds slots
+  // relative to each 256-token block; the dispatch adds local_base[b * R + r],
+  // writes the slot back to token_slot_out and counts num_tokens_per_expert
+  const int32_t *local_base = nullptr;
+  int32_t *token_slot_out = nullptr;
+  int32_t *num_tokens_per_expert = nullptr;
 };
 // early_rows of ep_get_layout_and_dispatch (the input stages and the output
 // buffers of the warp-specialised kernel hold up to 5 tokens)

@@ -239,6 +239,138 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_slot_kernel(LayoutParam
   if (tid == 0 && flags[0]) atomicOr(p.out.error_word, EP_ERRBIT_BAD_INDEX);
 }
 
+// ------------------------------------------------------------------------
+// The first half of a layout that the fp8 dispatch finishes (see
+// launch_layout_local).  One block per 256 tokens (one per thread): the rank
+// masks, each (token, rank)'s slot relative to the block (ballot prefix plus
+// a shared scan over warps, ascending token order), is_token_in_rank, and
+// the block's totals.  The last block to finish (a ticket on `done`, after a
+// fence) turns the totals into each block's first slot in each rank, in
+// place, and writes rank_prefix and num_tokens_per_rank; it leaves `done` at
+// zero for the next call.
+template <int KMAX>
+__global__ void __launch_bounds__(kLayoutThreads) layout_local_kernel(LayoutParams p, uint32_t *done) {
+  __shared__ int warp_off[kLayoutWarps * EP_MAX_RANKS];
+  __shared__ int blk_tot[EP_MAX_RANKS];
+  __shared__ int seg_sum[kLayoutThreads];
+  __shared__ int tot[EP_MAX_RANKS];
+  __shared__ int base[EP_MAX_RANKS + 1];
+  __shared__ int s_last;
+  const int tid = threadIdx.x;
+  const int lane = tid & (kWarpSize - 1);
+  const int warp = tid / kWarpSize;
+  const int G = gridDim.x;
+  const int b = blockIdx.x;
+  const int R = p.num_ranks, E = p.num_experts;
+  griddep_wait();
+  griddep_launch_dependents();
+  if (b == 0) {  // the dispatch adds into them, after this kernel
+    for (int i = tid; i < E; i += kLayoutThreads) p.out.num_tokens_per_expert[i] = 0;
+    if (tid == 0) *p.out.error_word = 0u;
+    if (tid < EP_WORK_COUNTER_WORDS && p.out.work_counters != nullptr) p.out.work_counters[tid] = 0u;
+  }
+  const int t = b * kLayoutThreads + tid;
+  int64_t ids[KMAX];
+  load_ids(p, t, p.num_tokens, ids);
+  bool bad = false;  // the dispatch reports bad ids
+  const uint64_t mask = rank_mask(ids, p.num_topk, E, p.experts_per_rank, nullptr, bad);
+  for (int r = 0; r < R; ++r) {
+    const uint32_t bal = __ballot_sync(0xffffffffu, (mask >> r) & 1ull);
+    if (lane == 0) warp_off[warp * R + r] = __popc(bal);
+  }
+  __syncthreads();
+  for (int r = tid; r < R; r += kLayoutThreads) {
+    int acc = 0;
+    for (int w = 0; w < kLayoutWarps; ++w) {
+      const int c = warp_off[w * R + r];
+      warp_off[w * R + r] = acc;
+      acc += c;
+    }
+    blk_tot[r] = acc;
+  }
+  __syncthreads();
+  const uint32_t lanes_below = (1u << lane) - 1u;
+  const bool vec4 = (R % 4) == 0;
+  int32_t *slot_row = p.out.token_slot + (size_t)t * R;
+  uint8_t *in_row = p.out.is_token_in_rank + (size_t)t * R;
+  for (int r0 = 0; r0 < R; r0 += 4) {
+    int sl[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = r0 + q;
+      sl[q] = -1;
+      if (r < R) {  // uniform across the warp
+        const bool in = (mask >> r) & 1ull;
+        const uint32_t bal = __ballot_sync(0xffffffffu, in);
+        if (in) sl[q] = warp_off[warp * R + r] + __popc(bal & lanes_below);
+      }
+    }
+    if (t < p.num_tokens) {
+      if (vec4) {
+        *reinterpret_cast<int4 *>(slot_row + r0) = make_int4(sl[0], sl[1], sl[2], sl[3]);
+        const uint32_t bytes = (sl[0] >= 0 ? 1u : 0u) | (sl[1] >= 0 ? 1u << 8 : 0u) |
+                               (sl[2] >= 0 ? 1u << 16 : 0u) | (sl[3] >= 0 ? 1u << 24 : 0u);
+        *reinterpret_cast<uint32_t *>(in_row + r0) = bytes;
+      } else {
+        for (int q = 0; q < 4 && r0 + q < R; ++q) {
+          slot_row[r0 + q] = sl[q];
+          in_row[r0 + q] = sl[q] >= 0 ? 1 : 0;
+        }
+      }
+    }
+  }
+  for (int r = tid; r < R; r += kLayoutThreads) p.partial[(size_t)b * R + r] = blk_tot[r];
+
+  // The last block: bases.  Thread (q, r) owns a contiguous run of blocks
+  // for rank r; run sums, then their exclusive scan, then the running bases.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(done, 1u) == (uint32_t)G - 1u;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int per_rank = kLayoutThreads / R;  // >= 4 since R <= 64
+  const int run_len = (G + per_rank - 1) / per_rank;
+  const int q = tid / R, r = tid % R;
+  const bool owner = tid < per_rank * R;
+  const int b0 = min(q * run_len, G), b1 = min(b0 + run_len, G);
+  if (owner) {
+    int sum = 0;
+    for (int bb = b0; bb < b1; ++bb) sum += __ldcg(&p.partial[(size_t)bb * R + r]);
+    seg_sum[tid] = sum;
+  }
+  __syncthreads();
+  for (int rr = tid; rr < R; rr += kLayoutThreads) {
+    int all = 0;
+    for (int qq = 0; qq < per_rank; ++qq) all += seg_sum[qq * R + rr];
+    tot[rr] = all;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int rr = 0; rr < R; ++rr) {
+      base[rr] = acc;
+      acc += tot[rr];
+    }
+    base[R] = acc;
+  }
+  __syncthreads();
+  for (int rr = tid; rr <= R; rr += kLayoutThreads) {
+    p.out.rank_prefix[rr] = base[rr];
+    if (rr < R) p.out.num_tokens_per_rank[rr] = tot[rr];
+  }
+  if (owner) {
+    int run = base[r];
+    for (int qq = 0; qq < q; ++qq) run += seg_sum[qq * R + r];
+    for (int bb = b0; bb < b1; ++bb) {
+      const int v = __ldcg(&p.partial[(size_t)bb * R + r]);
+      p.partial[(size_t)bb * R + r] = run;
+      run += v;
+    }
+  }
+  if (tid == 0) *done = 0u;
+}
+
 int max_layout_blocks(int num_tokens) {
   return std::max(1, (num_tokens + kLayoutThreads - 1) / kLayoutThreads);
 }
@@ -275,6 +407,32 @@ ep_status_t launch_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
   e = wide ? launch_kernel(layout_slot_kernel<EP_MAX_TOPK>, grid, kLayoutThreads, smem, stream, false, p)
            : launch_kernel(layout_slot_kernel<8>, grid, kLayoutThreads, smem, stream, false, p);
   if (e != cudaSuccess) return cuda_fail(e, "launch layout_slot_kernel");
+  return EP_OK;
+}
+
+int local_layout_max_tokens() { return kMaxLayoutBlocks * kLocalTokensPerBlock; }
+
+ep_status_t launch_layout_local(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
+                                int num_ranks, const ep_layout_t &layout, void *workspace, cudaStream_t stream,
+                                const int32_t **local_base) {
+  static_assert(kLocalTokensPerBlock == kLayoutThreads, "one token per thread");
+  LayoutParams p;
+  const int grid = (num_tokens + kLocalTokensPerBlock - 1) / kLocalTokensPerBlock;
+  p.topk_idx = topk_idx;
+  p.num_tokens = num_tokens;
+  p.num_topk = num_topk;
+  p.num_experts = num_experts;
+  p.num_ranks = num_ranks;
+  p.experts_per_rank = num_experts / num_ranks;
+  p.tokens_per_block = kLocalTokensPerBlock;
+  p.out = layout;
+  p.partial = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(workspace) + kPartialOffset);
+  uint32_t *done = static_cast<uint32_t *>(workspace);  // zero between calls
+  cudaError_t e = num_topk > 8
+                      ? launch_kernel(layout_local_kernel<EP_MAX_TOPK>, grid, kLayoutThreads, 0, stream, false, p, done)
+                      : launch_kernel(layout_local_kernel<8>, grid, kLayoutThreads, 0, stream, false, p, done);
+  if (e != cudaSuccess) return cuda_fail(e, "launch layout_local_kernel");
+  *local_base = p.partial;
   return EP_OK;
 }
 

@@ -123,11 +123,12 @@ typedef struct {
 } ep_layout_t;
 
 /*
- * Bytes of device workspace ep_get_layout needs for these sizes: the
- * per-block, per-rank token totals its two kernels exchange.  It needs no
- * initialisation (each call writes every total it reads) and can be reused
- * by later calls with any sizes up to the ones it was sized for.  Calls
- * sharing one workspace must be ordered (the same stream, or events).
+ * Bytes of device workspace ep_get_layout (and ep_get_layout_and_dispatch)
+ * needs for these sizes: the per-block, per-rank token totals the layout
+ * kernels exchange, after a 256-byte header.  Zero-fill it once when it is
+ * allocated; every call leaves the header zeroed again, so the workspace can
+ * be reused by later calls with any sizes up to the ones it was sized for.
+ * Calls sharing one workspace must be ordered (the same stream, or events).
  */
 size_t ep_layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
 
@@ -148,7 +149,7 @@ size_t ep_layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks)
  *   1 <= R <= EP_MAX_RANKS, R <= E <= EP_MAX_EXPERTS, E % R == 0.
  *   layout    every member non-null (token_slot 16-byte aligned).
  *   workspace >= ep_layout_workspace_bytes(T, E, R) bytes, 16-byte
- *             aligned (see above).
+ *             aligned, zero-filled at allocation (see above).
  */
 ep_status_t ep_get_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
                           int num_experts, int num_ranks,
@@ -290,8 +291,13 @@ ep_status_t ep_dispatch_ex(const ep_dispatch_args_t *args, ep_stream_t stream);
  * two launches, overlapped: the kernel ahead of the dispatch is known to be
  * the layout, which writes nothing the dispatch reads first, so with fp8
  * rows each dispatch block loads and casts the rows of its first tokens
- * while the layout still runs, and waits for it only to store them.  Every
- * output of both calls is written, identical to the two calls.
+ * while the layout still runs, and waits for it only to store them.  With
+ * fp8 rows and 0 < T <= 524,288 the layout is one launch: it writes
+ * is_token_in_rank, rank_prefix, num_tokens_per_rank and each slot relative
+ * to its block of 256 tokens, and the dispatch adds each block's base as it
+ * moves the token, writes the final slot back and counts
+ * num_tokens_per_expert (and bad ids).  Every output of both calls is
+ * written, identical to the two calls.
  *   args       as for ep_dispatch_ex; every array of *args->layout is
  *              written (as ep_get_layout), so its token_slot and
  *              is_token_in_rank must be 16-byte aligned.
