@@ -356,7 +356,9 @@ def run_ours(args, rank, world, local):
         barrier(world)
     ms_per_step = ev0.elapsed_time(ev1) / args.steps
     ms_per_step = max_over_ranks(ms_per_step, world)
-    launches = 4 * args.steps  # layout (count, slots), dispatch, combine
+    # layout (one launch for fp8 rows up to 524 288 tokens, else count and
+    # slots), dispatch, combine
+    launches = (3 if cfg.fp8 and 0 < T <= 2048 * 256 else 4) * args.steps
 
     # (2) the same steps with an event between kernels: per-kernel durations.
     k_steps = min(args.steps, 500)
