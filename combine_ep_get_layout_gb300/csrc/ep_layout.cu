@@ -17,6 +17,10 @@
 //            first slot in each rank), then warp ballots and a shared scan
 //            over warps give each (token, rank) its slot in ascending token
 //            order (a stable scatter).
+//
+// layout_local_kernel is the one-launch layout of ep_get_layout_and_dispatch
+// (fp8 rows): slots relative to each 256-token block, and the blocks' bases
+// from the last block to finish; the dispatch adds the bases.
 #include <algorithm>
 
 #include "ep_device.cuh"
@@ -26,7 +30,7 @@ namespace {
 
 constexpr int kLayoutThreads = 256;  // one token per thread per chunk
 constexpr int kLayoutWarps = kLayoutThreads / kWarpSize;
-constexpr size_t kPartialOffset = 256;  // bytes of the workspace before the block totals (unused)
+constexpr size_t kPartialOffset = 256;  // workspace header (the local layout's ticket word), then the totals
 constexpr int kMaxLayoutBlocks = 2048;  // more tokens per block beyond this
 
 struct LayoutParams {
@@ -37,8 +41,8 @@ struct LayoutParams {
   int32_t *partial;  // [gridDim.x * R] per-block, per-rank token counts
 };
 
-// The rank mask of token t (ids of row `ids`), the count of each valid id in
-// `hist` (shared; null to skip) and `bad` for an id outside [-1, E).
+// The rank mask of a token whose ids are `ids`; counts each valid id in
+// `hist` (shared; null to skip) and sets `bad` for an id outside [-1, E).
 template <int KMAX>
 __device__ __forceinline__ uint64_t rank_mask(const int64_t (&ids)[KMAX], int K, int E, int epr, int *hist,
                                               bool &bad) {
@@ -58,6 +62,8 @@ __device__ __forceinline__ uint64_t rank_mask(const int64_t (&ids)[KMAX], int K,
   return mask;
 }
 
+// The K ids of token t, all requested before the first is used; -1 past K
+// and for t >= end.
 template <int KMAX>
 __device__ __forceinline__ void load_ids(const LayoutParams &p, int t, int end, int64_t (&ids)[KMAX]) {
   const int64_t *row = p.topk_idx + (size_t)t * p.num_topk;
