@@ -297,7 +297,9 @@ ep_status_t ep_dispatch_ex(const ep_dispatch_args_t *args, ep_stream_t stream);
  * to its block of 256 tokens, and the dispatch adds each block's base as it
  * moves the token, writes the final slot back and counts
  * num_tokens_per_expert (and bad ids).  Every output of both calls is
- * written, identical to the two calls.
+ * written, identical to the two calls (on that path, if the dispatch gives
+ * up with EP_ERRBIT_TIMEOUT, the tokens it did not reach keep their
+ * block-relative slots and are not counted).
  *   args       as for ep_dispatch_ex; every array of *args->layout is
  *              written (as ep_get_layout), so its token_slot and
  *              is_token_in_rank must be 16-byte aligned.
