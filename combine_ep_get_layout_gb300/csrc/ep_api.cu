@@ -236,7 +236,7 @@ ep_status_t ep_get_layout_and_dispatch(const ep_dispatch_args_t *args, void *wor
   if (workspace_bytes < need)
     return fail(EP_ERR_INVALID_ARG, "%s: workspace_bytes=%zu < %zu needed", fn, workspace_bytes, need);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (a.fp8 && a.num_tokens > 0 && a.num_tokens <= local_layout_max_tokens()) {
+  if ((a.fp8 || kBf16WarpSpecialised) && a.num_tokens > 0 && a.num_tokens <= local_layout_max_tokens()) {
     // One layout launch; the dispatch finishes the slots (adds each block's
     // base, writes them back) and counts the experts as it moves the rows.
     const int32_t *local_base = nullptr;

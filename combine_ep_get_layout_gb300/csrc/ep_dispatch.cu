@@ -412,6 +412,9 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(Dispatc
 
 constexpr int kWsCasters = 8;
 constexpr int kWsThreads = (2 + kWsCasters) * kWarpSize;
+constexpr int kWsBf16Threads = 2 * kWarpSize;  // loader and storer
+constexpr int kWsBf16Stages = 8;                // bf16 row stages (fewer for wide rows)
+constexpr size_t kWsBf16SmemBudget = 64 * 1024;
 constexpr int kWsOut = 3;
 // The storer releases an output buffer one token late (once the next
 // token's stores are issued), so waiting for the stores to read a buffer
@@ -433,7 +436,11 @@ __device__ __forceinline__ void release_out(uint64_t *empty_out, int i, int lane
   }
 }
 
-__global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams p) {
+// CAST: fp8 rows (casters between the loader and the storer); otherwise
+// bf16 rows, which the storer bulk-stores straight from the input stage
+// (two warps, no casters, no output buffers).
+template <bool CAST>
+__device__ __forceinline__ void dispatch_ws_body(const DispatchParams &p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int S = p.stages;
   uint64_t *full_in = reinterpret_cast<uint64_t *>(smem);  // [S]
@@ -455,7 +462,7 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_in[s], 1);
-      mbar_init(&empty_in[s], kWsCasters);
+      mbar_init(&empty_in[s], CAST ? kWsCasters : 1);
     }
     for (int o = 0; o < kWsOut; ++o) {
       mbar_init(&full_out[o], kWsCasters);
@@ -467,7 +474,7 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
   if (p.packed) {  // the padding of both packed output rows stays zero
     const uint32_t used = (uint32_t)p.H + (uint32_t)p.groups * 4u;
     for (int o = 0; o < kWsOut; ++o)
-      for (uint32_t b = used + tid; b < p.row_out_bytes; b += kWsThreads) out[(size_t)o * p.out_stride + b] = 0;
+      for (uint32_t b = used + tid; b < p.row_out_bytes; b += blockDim.x) out[(size_t)o * p.out_stride + b] = 0;
     fence_proxy_async_smem();
   }
   __syncthreads();
@@ -583,6 +590,30 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
           if (p.recv_topk_weights != nullptr) p.recv_topk_weights[(size_t)slot * p.K + lane] = here ? w : 0.0f;
         }
       }
+      if constexpr (!CAST) {  // bf16: the row goes out from its input stage
+        const int s = i % S;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full_in[s], (uint32_t)(i / S) & 1u))) {
+          if (lane == 0) {
+            *s_abort = 1;
+            set_error(p.error_word, EP_ERRBIT_TIMEOUT);
+          }
+          break;
+        }
+        if (lane == 0) s_tok[i % kTokRing] = kTokPending;
+        const unsigned char *stage = in + (size_t)s * p.stage_stride;
+        if (slot_lo >= 0)
+          bulk_store(static_cast<unsigned char *>(p.recv_x) + (size_t)slot_lo * p.row_out_bytes, stage,
+                     p.row_out_bytes);
+        if (slot_hi >= 0)
+          bulk_store(static_cast<unsigned char *>(p.recv_x) + (size_t)slot_hi * p.row_out_bytes, stage,
+                     p.row_out_bytes);
+        bulk_commit();
+        // the stores of token i-1 have read their stage: the loader may refill it
+        bulk_wait_read<1>();
+        __syncwarp();
+        if (lane == 0 && i > 0) mbar_arrive(&empty_in[(i - 1) % S]);
+        continue;
+      }
       const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full_out[o], (uint32_t)(i / kWsOut) & 1u));
       if (!ok) {
         if (lane == 0) {
@@ -630,7 +661,7 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
       release_out(empty_out, i, lane);
     }
     bulk_wait<0>();
-  } else {
+  } else if (CAST) {
     const int cw = warp - 2;
     for (int i = 0; !*s_abort; ++i) {
       const int s = i % S;
@@ -676,6 +707,11 @@ __global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams 
   }
 }
 
+__global__ void __launch_bounds__(kWsThreads) dispatch_ws_kernel(DispatchParams p) { dispatch_ws_body<true>(p); }
+__global__ void __launch_bounds__(kWsBf16Threads) dispatch_ws_bf16_kernel(DispatchParams p) {
+  dispatch_ws_body<false>(p);
+}
+
 size_t ws_smem_bytes(const DispatchParams &p) {
   return kHeaderBytes + (size_t)p.stages * p.stage_stride + kWsOut * ((size_t)p.out_stride + p.scale_stride);
 }
@@ -704,6 +740,36 @@ ep_status_t launch_ws(DispatchParams &p, const DeviceInfo &di, cudaStream_t stre
   const int grid = std::min(p.T, per_sm * di.num_sms);
   e = launch_kernel(dispatch_ws_kernel, grid, kWsThreads, smem, stream, false, p);
   if (e != cudaSuccess) return cuda_fail(e, "launch dispatch_ws_kernel");
+  return EP_OK;
+}
+
+// bf16 rows through the warp-specialised kernel's loader and storer.
+ep_status_t launch_ws_bf16(DispatchParams &p, const DeviceInfo &di, cudaStream_t stream) {
+  static std::mutex mu;
+  static bool configured[64] = {};
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (di.device < 64 && !configured[di.device]) {
+      cudaError_t e = cudaFuncSetAttribute(dispatch_ws_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)di.max_smem_per_block_optin);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(dispatch_ws_bf16_kernel)");
+      configured[di.device] = true;
+    }
+  }
+  auto smem_of = [&](int stages) { return kHeaderBytes + (size_t)stages * p.stage_stride; };
+  p.stages = kWsBf16Stages;
+  while (p.stages > 2 && smem_of(p.stages) > kWsBf16SmemBudget) --p.stages;
+  const size_t smem = smem_of(p.stages);
+  if (smem > di.max_smem_per_block_optin)
+    return fail(EP_ERR_UNSUPPORTED, "ep_dispatch: hidden %d needs %zu bytes of shared memory", p.H, smem);
+  int per_sm = 0;
+  cudaError_t e =
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_ws_bf16_kernel, kWsBf16Threads, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(dispatch_ws_bf16)");
+  if (per_sm <= 0) return fail(EP_ERR_UNSUPPORTED, "ep_dispatch: kernel cannot be resident");
+  const int grid = std::min(p.T, per_sm * di.num_sms);
+  e = launch_kernel(dispatch_ws_bf16_kernel, grid, kWsBf16Threads, smem, stream, false, p);
+  if (e != cudaSuccess) return cuda_fail(e, "launch dispatch_ws_bf16_kernel");
   return EP_OK;
 }
 
@@ -899,7 +965,8 @@ ep_status_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream) {
       st = (kFp8WarpSpecialised || p.packed || p.local_base != nullptr) ? launch_ws(p, *di, stream)
                                                                          : launch_ring<true>(p, *di, stream);
     else
-      st = launch_ring<false>(p, *di, stream);
+      st = (kBf16WarpSpecialised && !p.expanded) || p.local_base != nullptr ? launch_ws_bf16(p, *di, stream)
+                                                                            : launch_ring<false>(p, *di, stream);
   }
   if (st == EP_OK && pad) st = launch_pad(p, *di, stream);
   return st;

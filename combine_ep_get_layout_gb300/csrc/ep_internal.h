@@ -101,6 +101,9 @@ struct DispatchArgs {
 // early_rows of ep_get_layout_and_dispatch (the input stages and the output
 // buffers of the warp-specialised kernel hold up to 5 tokens)
 constexpr int kEarlyRows = 3;
+// bf16 rows of the rank path through the warp-specialised kernel (else the
+// ring kernel); the one-launch layout of ep_get_layout_and_dispatch needs it
+constexpr bool kBf16WarpSpecialised = true;
 ep_status_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream);
 
 // ---- combine (ep_combine.cu)
