@@ -68,13 +68,13 @@ KERNEL_SOURCES = {
 }
 def kernel_symbol(kernel: str, cfg: W.EPConfig) -> str:
     """The library kernel(s) that run each call for this workload (the
-    layout is two kernels; the library picks the warp-specialised fp8
-    dispatch, the ring kernel for bf16, and the warp-specialised combine for
-    up to 8 ranks)."""
+    layout is two kernels; the library picks the warp-specialised dispatch,
+    with the fp8 cast or without it for bf16, and the warp-specialised
+    combine for up to 8 ranks)."""
     if kernel == "layout":
         return "layout_count_kernel+layout_slot_kernel"
     if kernel == "dispatch":
-        return "dispatch_ws_kernel" if cfg.fp8 else "dispatch_ring_kernel"
+        return "dispatch_ws_kernel" if cfg.fp8 else "dispatch_ws_bf16_kernel"
     return "combine_ws_kernel" if cfg.num_ranks <= 8 else "combine_kernel"
 
 
@@ -356,9 +356,9 @@ def run_ours(args, rank, world, local):
         barrier(world)
     ms_per_step = ev0.elapsed_time(ev1) / args.steps
     ms_per_step = max_over_ranks(ms_per_step, world)
-    # layout (one launch for fp8 rows up to 524 288 tokens, else count and
-    # slots), dispatch, combine
-    launches = (3 if cfg.fp8 and 0 < T <= 2048 * 256 else 4) * args.steps
+    # layout (one launch up to 524 288 tokens, else count and slots),
+    # dispatch, combine
+    launches = (3 if 0 < T <= 2048 * 256 else 4) * args.steps
 
     # (2) the same steps with an event between kernels: per-kernel durations.
     k_steps = min(args.steps, 500)

@@ -289,10 +289,10 @@ ep_status_t ep_dispatch_ex(const ep_dispatch_args_t *args, ep_stream_t stream);
  * the scatter of TileScale PR #68 issued together (same page, commit
  * messages fusing the layout back into the dispatch).  The work is the same
  * two launches, overlapped: the kernel ahead of the dispatch is known to be
- * the layout, which writes nothing the dispatch reads first, so with fp8
- * rows each dispatch block loads and casts the rows of its first tokens
+ * the layout, which writes nothing the dispatch reads first, so each
+ * dispatch block loads (and for fp8 casts) the rows of its first tokens
  * while the layout still runs, and waits for it only to store them.  With
- * fp8 rows and 0 < T <= 524,288 the layout is one launch: it writes
+ * 0 < T <= 524,288 the layout is one launch: it writes
  * is_token_in_rank, rank_prefix, num_tokens_per_rank and each slot relative
  * to its block of 256 tokens, and the dispatch adds each block's base as it
  * moves the token, writes the final slot back and counts
