@@ -311,3 +311,34 @@ def test_token_order_modes(name, work_counters):
         assert g["work_counters"].tolist() == [0, 0, 0, 0]
     else:
         assert g["work_counters"] is None
+
+
+def test_weighted_combine_with_a_wider_routings_layout():
+    """A layout of a wider routing (top-8 over 8 ranks) combined with a top-2
+    routing: tokens with more rank rows than two experts can reach are
+    flagged as a stale layout; tokens whose rank sets agree with the layout
+    still combine exactly as the oracle does."""
+    T, H, E, R = 2048, 512, 64, 8
+    epr = E // R
+    rng = np.random.default_rng(21)
+    wide = np.argsort(rng.random((T, E)), axis=1)[:, :8].astype(np.int64)
+    for t in range(T // 2):  # these tokens: all 8 experts on two ranks, so top-2 below agrees
+        r1, r2 = rng.choice(R, 2, replace=False)
+        wide[t] = np.stack([r1 * epr + rng.choice(epr, 4, replace=False),
+                            r2 * epr + rng.choice(epr, 4, replace=False)], axis=1).reshape(8)
+    lay = ep.ep_get_layout(torch.from_numpy(wide).to(U.dev()), E, R)
+    torch.cuda.synchronize()
+    lo = oracle.get_layout(wide, E, R)
+    N = int(lo["rank_prefix"][R])
+    y_bits = W.expert_output(N, H)
+    narrow = wide[:, :2].copy()
+    w2 = rng.random((T, 2)).astype(np.float32)
+    out = ep.ep_combine(U.to_dev_bf16(y_bits), lay, torch.from_numpy(narrow).to(U.dev()),
+                        torch.from_numpy(w2).to(U.dev()))
+    torch.cuda.synchronize()
+    assert lay.errors() & ep.EP_ERRBIT_STALE_LAYOUT
+    agree = np.array([set((wide[t] // epr).tolist()) == set((narrow[t] // epr).tolist()) for t in range(T)])
+    assert agree.any() and (~agree).any()
+    want, _ = oracle.combine(y_bits, lo["token_slot"], narrow, w2, E)
+    got = U.bits(out)
+    assert np.array_equal(got[agree], want[agree])
