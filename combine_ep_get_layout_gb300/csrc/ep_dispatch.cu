@@ -4,19 +4,18 @@
 // cast fused into the same pass (same page, commit message on packing the
 // fp8 row; DeepEP's per_token_cast_to_fp8 layout).
 //
-// dispatch_ring_kernel: one CTA works through its tokens
-// (t = blockIdx.x + i * gridDim.x) with a ring of `stages` shared-memory row
-// buffers:
-//   - a bulk (TMA 1D) copy brings token i's bf16 row into its stage, signalled
-//     on an mbarrier; loads run `stages - 1` tokens ahead;
-//   - bf16: warp 0 issues one bulk store of the stage per destination rank,
-//     straight to recv_x[token_slot[t][r]];
-//   - fp8: every warp casts 128-element groups (amax by warp shuffles,
-//     scale = amax / 448, e4m3 round-to-nearest-even with saturation) into a
-//     double-buffered output row, then warp 0 bulk-stores it per destination;
-//   - the other warps write the received metadata (source token, local expert
-//     ids, gate weights) and, for fp8, the scales.
-// Each row of x is read from HBM once and written once per destination rank.
+// dispatch_ws_kernel (fp8 rows) and dispatch_ws_bf16_kernel (bf16 rows):
+// warp-specialised, a loader warp bulk-loading rows into a ring of input
+// stages, for fp8 eight caster warps, and a storer warp writing the received
+// metadata and bulk-storing each row to every destination slot, handing
+// buffers over through mbarriers (details above the kernel body below).
+//
+// dispatch_ring_kernel (bf16 rows of an expanded layout): one CTA works
+// through its tokens with a ring of `stages` shared-memory row buffers;
+// thread 0 draws tokens and bulk-loads their rows, warp 0 issues one bulk
+// store of the stage per destination, the other warps write the metadata.
+//
+// Each row of x is read from HBM once and written once per destination.
 #include <algorithm>
 #include <climits>
 #include <mutex>
@@ -27,13 +26,11 @@ namespace ep {
 namespace {
 
 constexpr int kDispatchThreads = 256;
-constexpr int kDispatchWarps = kDispatchThreads / kWarpSize;
 constexpr int kMaxStages = 8;
 constexpr int kHeaderBytes = 1024;  // mbarriers, flags, slot buffers
 constexpr size_t kSmemBudget = 80 * 1024;  // per CTA: aims at >= 2-3 CTAs per SM
 constexpr int kWsStages = 2;                 // bf16 row stages of the fp8 kernel
 constexpr size_t kWsSmemBudget = 64 * 1024;
-constexpr bool kFp8WarpSpecialised = true;
 constexpr bool kWsWarmL2 = true;  // fp8 kernel: L2 hints before the grid-dependency wait
 
 struct DispatchParams {
@@ -144,11 +141,8 @@ __device__ __forceinline__ int local_expert(const DispatchParams &p, int64_t e) 
 }
 
 // Received metadata of token t, by threads [32, blockDim): source token,
-// local expert ids and gate weights of every row the token is sent as, and
-// for fp8 the row's scales.
-template <bool FP8>
-__device__ __forceinline__ void write_metadata(const DispatchParams &p, int t,
-                                               const int32_t *slots, const float *scales) {
+// local expert ids and gate weights of every row the token is sent as.
+__device__ __forceinline__ void write_metadata(const DispatchParams &p, int t, const int32_t *slots) {
   const int mt = threadIdx.x - kWarpSize;
   const int nt = kDispatchThreads - kWarpSize;
   if (threadIdx.x / kWarpSize == 1) {  // warp 1 checks the layout against the routing
@@ -177,15 +171,6 @@ __device__ __forceinline__ void write_metadata(const DispatchParams &p, int t,
       if (p.recv_topk_idx != nullptr) p.recv_topk_idx[(size_t)slot * p.K + k] = here ? local_expert(p, e) : -1;
       if (p.recv_topk_weights != nullptr)
         p.recv_topk_weights[(size_t)slot * p.K + k] = here ? __ldg(p.topk_weights + (size_t)t * p.K + k) : 0.0f;
-    }
-  }
-  if constexpr (FP8) {
-    const int DG = p.D * p.groups;
-    for (int q = mt; q < DG; q += nt) {
-      const int j = q / p.groups;
-      const int g = q - j * p.groups;
-      const int slot = slots[j];
-      if (slot >= 0 && slot < p.cap) p.recv_x_scales[(size_t)slot * p.groups + g] = scales[g];
     }
   }
 }
@@ -268,7 +253,6 @@ __device__ __forceinline__ void cast_two_groups(const unsigned char *stage, unsi
   }
 }
 
-template <bool FP8>
 __global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(DispatchParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);               // [kMaxStages]
@@ -276,8 +260,6 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(Dispatc
   int32_t *s_slot = reinterpret_cast<int32_t *>(smem + 128);         // [2][EP_MAX_RANKS]
   volatile int *s_tok = reinterpret_cast<volatile int *>(smem + 640);  // [kTokRing]
   unsigned char *stages = smem + kHeaderBytes;
-  unsigned char *obuf = stages + (size_t)p.stages * p.stage_stride;  // fp8: [2][out_stride]
-  float *sbuf = reinterpret_cast<float *>(obuf + 2 * (size_t)p.out_stride);  // fp8: [2][groups]
 
   const int tid = threadIdx.x;
   const int warp = tid / kWarpSize;
@@ -319,41 +301,10 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(Dispatc
     unsigned char *stage = stages + (size_t)s * p.stage_stride;
 
     if (tid < p.D) slots[tid] = __ldg(p.token_slot + (size_t)t * p.D + tid);
-    if constexpr (FP8) {
-      // the stores of token i-2 read obuf[b]: let them finish reading it
-      if (warp == 0) bulk_wait_read<1>();
-    }
     __syncthreads();
     if (*s_abort) break;
 
-    if constexpr (FP8) {
-      if (!mbar_wait_bounded(&full[s], parity)) {
-        *s_abort = 1;
-        if (lane == 0) set_error(p.error_word, EP_ERRBIT_TIMEOUT);
-      }
-      unsigned char *orow = obuf + (size_t)b * p.out_stride;
-      float *srow = sbuf + (size_t)b * (p.scale_stride / 4);
-      for (int g0 = 2 * warp; g0 < p.groups; g0 += 2 * kDispatchWarps)
-        cast_two_groups(stage, orow, srow, g0, p.groups, lane);
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (*s_abort) break;
-      if (warp == 0) {
-        if (lane == 0 && !drained) issue_token(p, stages, full, s_tok, issued++, drained, policy);
-        for (int j = lane; j < p.D; j += kWarpSize) {
-          const int slot = slots[j];
-          if (slot < 0) continue;
-          if (slot < p.cap)
-            bulk_store(static_cast<unsigned char *>(p.recv_x) + (size_t)slot * p.row_out_bytes, orow,
-                       p.row_out_bytes);
-          else
-            set_error(p.error_word, EP_ERRBIT_CAPACITY);
-        }
-        bulk_commit();
-      } else {
-        write_metadata<true>(p, t, slots, srow);
-      }
-    } else {
+    {
       if (warp == 0) {
         const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], parity));
         if (!ok) {
@@ -378,7 +329,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(Dispatc
           if (lane == 0 && i >= 1 && !drained) issue_token(p, stages, full, s_tok, issued++, drained, policy);
         }
       } else {
-        write_metadata<false>(p, t, slots, nullptr);
+        write_metadata(p, t, slots);
       }
     }
   }
@@ -396,7 +347,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(Dispatc
 
 
 // ------------------------------------------------------------------------
-// Warp-specialised fp8 kernel.  Roles inside one CTA, handing buffers over
+// Warp-specialised kernel.  Roles inside one CTA, handing buffers over
 // through mbarriers (no CTA-wide barrier in the loop):
 //   warp 0 (loader)    bulk-loads token rows into a ring of `stages` bf16
 //                      row buffers (full_in), reusing a buffer once every
@@ -405,10 +356,12 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(Dispatc
 //                      cast row and its scales to every destination slot
 //                      (full_out), releasing the buffer once the stores have
 //                      read it (empty_out);
-//   warps 2.. (casters) cast 128-element groups of a row into one of two
+//   warps 2.. (casters) cast 128-element groups of a row into one of three
 //                      fp8 row buffers.
 // Casting token i+1 thus overlaps the stores of token i and the loads of
-// the tokens after it.
+// the tokens after it.  For bf16 rows (dispatch_ws_bf16_kernel) there are
+// no casters: the storer stores each row from its input stage and releases
+// the stage (empty_in) one token late, once those stores have read it.
 
 constexpr int kWsCasters = 8;
 constexpr int kWsThreads = (2 + kWsCasters) * kWarpSize;
@@ -877,20 +830,16 @@ ep_status_t launch_pad(const DispatchParams &p, const DeviceInfo &di, cudaStream
   return EP_OK;
 }
 
-size_t dispatch_smem_bytes(const DispatchParams &p, bool fp8) {
-  size_t bytes = kHeaderBytes + (size_t)p.stages * p.stage_stride;
-  if (fp8) bytes += 2 * (size_t)p.out_stride + 2 * (size_t)p.scale_stride;
-  return bytes;
-}
+size_t dispatch_smem_bytes(const DispatchParams &p) { return kHeaderBytes + (size_t)p.stages * p.stage_stride; }
 
-template <bool FP8>
+// bf16 rows of an expanded layout.
 ep_status_t launch_ring(DispatchParams &p, const DeviceInfo &di, cudaStream_t stream) {
   static std::mutex mu;
   static bool configured[64] = {};
   {
     std::lock_guard<std::mutex> g(mu);
     if (di.device < 64 && !configured[di.device]) {
-      cudaError_t e = cudaFuncSetAttribute(dispatch_ring_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaError_t e = cudaFuncSetAttribute(dispatch_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)di.max_smem_per_block_optin);
       if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(dispatch_ring_kernel)");
       configured[di.device] = true;
@@ -898,17 +847,17 @@ ep_status_t launch_ring(DispatchParams &p, const DeviceInfo &di, cudaStream_t st
   }
   // Deepest ring that keeps the CTA within budget (at least 2 stages).
   p.stages = kMaxStages > 4 ? 4 : kMaxStages;
-  while (p.stages > 2 && dispatch_smem_bytes(p, FP8) > kSmemBudget) --p.stages;
-  const size_t smem = dispatch_smem_bytes(p, FP8);
+  while (p.stages > 2 && dispatch_smem_bytes(p) > kSmemBudget) --p.stages;
+  const size_t smem = dispatch_smem_bytes(p);
   if (smem > di.max_smem_per_block_optin)
     return fail(EP_ERR_UNSUPPORTED, "ep_dispatch: hidden %d needs %zu bytes of shared memory", p.H, smem);
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_ring_kernel<FP8>,
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_ring_kernel,
                                                                 kDispatchThreads, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(dispatch)");
   if (per_sm <= 0) return fail(EP_ERR_UNSUPPORTED, "ep_dispatch: kernel cannot be resident");
   const int grid = std::min(p.T, per_sm * di.num_sms);
-  e = launch_kernel(dispatch_ring_kernel<FP8>, grid, kDispatchThreads, smem, stream, false, p);
+  e = launch_kernel(dispatch_ring_kernel, grid, kDispatchThreads, smem, stream, false, p);
   if (e != cudaSuccess) return cuda_fail(e, "launch dispatch_ring_kernel");
   return EP_OK;
 }
@@ -962,11 +911,10 @@ ep_status_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream) {
   if (a.num_tokens > 0) {
     // packed rows are only built by the warp-specialised kernel
     if (a.fp8)
-      st = (kFp8WarpSpecialised || p.packed || p.local_base != nullptr) ? launch_ws(p, *di, stream)
-                                                                         : launch_ring<true>(p, *di, stream);
+      st = launch_ws(p, *di, stream);
     else
       st = (kBf16WarpSpecialised && !p.expanded) || p.local_base != nullptr ? launch_ws_bf16(p, *di, stream)
-                                                                            : launch_ring<false>(p, *di, stream);
+                                                                            : launch_ring(p, *di, stream);
   }
   if (st == EP_OK && pad) st = launch_pad(p, *di, stream);
   return st;
