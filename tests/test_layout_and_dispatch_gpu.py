@@ -98,6 +98,12 @@ CASES = [
     ("packed_stats", 3000, 640, 5, 20, 5, "fp8_packed", {}),
     ("fp8_stripes", 3000, 1024, 8, 64, 8, "fp8", dict(work_counters=False)),
     ("bf16_rows", 1000, 256, 6, 64, 8, "bf16", {}),
+    ("bf16_T1", 1, 64, 2, 8, 2, "bf16", {}),
+    ("bf16_R64_K32", 700, 512, 32, 128, 64, "bf16", {}),
+    ("bf16_R5_H8", 900, 8, 3, 20, 5, "bf16", {}),
+    ("bf16_wide_rows", 300, 16384, 8, 64, 8, "bf16", {}),
+    ("bf16_bad_ids_stripes", 2000, 256, 6, 32, 8, "bf16", dict(bad=0.03, work_counters=False)),
+    ("bf16_all_masked", 500, 256, 4, 16, 4, "bf16", dict(p_mask=1.0)),
     ("fp8_T0", 0, 256, 4, 16, 4, "fp8", {}),
     ("fp8_fewer_tokens_than_blocks", 37, 7168, 8, 256, 8, "fp8", {}),
     ("fp8_about_3_tokens_per_block", 1900, 1024, 8, 64, 8, "fp8", {}),
