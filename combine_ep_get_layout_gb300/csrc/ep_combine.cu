@@ -254,6 +254,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
 // the per-token metadata or on the reduction.
 
 constexpr int kWsMaxRanks = 8;
+constexpr int kSmallStageRows = 6;
 // L2 warm-up before the grid-dependency wait: tokens per block, leading
 // chunks of each of their rows
 constexpr int kWarmTokens = 2;
@@ -264,7 +265,6 @@ constexpr int kReducers = 8;                   // warps
 constexpr int kWsCombineThreads = (1 + kReducers) * kWarpSize;
 constexpr int kCombineStages = 2;
 constexpr int kStageHeader = 128;              // n, coefficients
-constexpr int kStageBytes = kStageHeader + kWsMaxRanks * kChunkBytes;
 
 // One token's routing as the loader warp holds it: lane r < R has the slot
 // of rank r, lane k < K the k-th expert id and gate weight.
@@ -282,8 +282,12 @@ __device__ __forceinline__ TokenMeta fetch_meta(const CombineParams &p, int t, i
   return m;
 }
 
-template <bool WEIGHTED>
+// ROWS: the rows a stage holds, the most a token can have (6 when a
+// routing of at most 6 experts per token is given: smaller stages, four
+// blocks per SM; else kWsMaxRanks).
+template <bool WEIGHTED, int ROWS>
 __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombineParams p) {
+  constexpr int kStageBytes = kStageHeader + ROWS * kChunkBytes;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [kCombineStages]
   uint64_t *empty = full + kCombineStages;              // [kCombineStages]
@@ -363,8 +367,13 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
       }
       const float coef = WEIGHTED ? coefficient(p, cur.e, cur.w, lane) : 1.0f;
       const uint32_t bal = __ballot_sync(0xffffffffu, slot >= 0);
-      const int nrows = __popc(bal);
+      int nrows = __popc(bal);
       const int pos = row_position(p, slot, bal, lanes_below);
+      if (nrows > ROWS) {  // more ranks than the routing can reach: a layout of another routing
+        if (lane == 0) set_error(p.error_word, EP_ERRBIT_STALE_LAYOUT);
+        if (pos >= ROWS) slot = -1;
+        nrows = ROWS;
+      }
       for (int c = 0; c < nchunk; ++c, ++i) {
         const int s = static_cast<int>(i % kCombineStages);
         const int elems = min(kChunk, p.H - c * kChunk);
@@ -477,29 +486,39 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
   }
 }
 
-template <bool WEIGHTED>
-ep_status_t launch_ws(const CombineParams &p, const DeviceInfo &di, cudaStream_t stream) {
+template <bool WEIGHTED, int ROWS>
+ep_status_t launch_ws_rows(const CombineParams &p, const DeviceInfo &di, cudaStream_t stream) {
   static std::mutex mu;
   static bool configured[64] = {};
-  const size_t smem = 128 + (size_t)kCombineStages * kStageBytes;
+  const auto kernel = combine_ws_kernel<WEIGHTED, ROWS>;
+  const size_t smem = 128 + (size_t)kCombineStages * (kStageHeader + (size_t)ROWS * kChunkBytes);
   {
     std::lock_guard<std::mutex> g(mu);
     if (di.device < 64 && !configured[di.device]) {
-      cudaError_t e = cudaFuncSetAttribute(combine_ws_kernel<WEIGHTED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(combine_ws_kernel)");
       configured[di.device] = true;
     }
   }
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_ws_kernel<WEIGHTED>,
-                                                                kWsCombineThreads, smem);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kWsCombineThreads, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(combine_ws)");
   if (per_sm <= 0) return fail(EP_ERR_UNSUPPORTED, "ep_combine: kernel cannot be resident");
   const int grid = std::min(p.T, per_sm * di.num_sms);
-  e = launch_kernel(combine_ws_kernel<WEIGHTED>, grid, kWsCombineThreads, smem, stream, false, p);
+  e = launch_kernel(kernel, grid, kWsCombineThreads, smem, stream, false, p);
   if (e != cudaSuccess) return cuda_fail(e, "launch combine_ws_kernel");
   return EP_OK;
+}
+
+// A token has at most min(K, R) rank rows under a given routing: with at
+// most 6, stages of 6 rows (four blocks per SM instead of three).
+template <bool WEIGHTED>
+ep_status_t launch_ws(const CombineParams &p, const DeviceInfo &di, cudaStream_t stream) {
+  if constexpr (WEIGHTED) {
+    if (!p.expanded && std::min(p.K, p.D) <= kSmallStageRows)
+      return launch_ws_rows<WEIGHTED, kSmallStageRows>(p, di, stream);
+  }
+  return launch_ws_rows<WEIGHTED, kWsMaxRanks>(p, di, stream);
 }
 
 constexpr bool kUseWsCombine = true;
