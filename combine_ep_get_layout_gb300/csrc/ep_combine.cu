@@ -255,6 +255,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
 
 constexpr int kWsMaxRanks = 8;
 constexpr int kSmallStageRows = 6;
+constexpr int kSplitMinTokens = 32768;
 // L2 warm-up before the grid-dependency wait: tokens per block, leading
 // chunks of each of their rows
 constexpr int kWarmTokens = 2;
@@ -285,7 +286,10 @@ __device__ __forceinline__ TokenMeta fetch_meta(const CombineParams &p, int t, i
 // ROWS: the rows a stage holds, the most a token can have (6 when a
 // routing of at most 6 experts per token is given: smaller stages, four
 // blocks per SM; else kWsMaxRanks).
-template <bool WEIGHTED, int ROWS>
+// SPLIT: a token with more rows than a stage holds goes as two units per
+// chunk, the first carrying its sum on to the second (else a stage holds
+// every row a token can have).
+template <bool WEIGHTED, int ROWS, bool SPLIT>
 __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombineParams p) {
   constexpr int kStageBytes = kStageHeader + ROWS * kChunkBytes;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -369,34 +373,42 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
       const uint32_t bal = __ballot_sync(0xffffffffu, slot >= 0);
       int nrows = __popc(bal);
       const int pos = row_position(p, slot, bal, lanes_below);
-      if (nrows > ROWS) {  // more ranks than the routing can reach: a layout of another routing
+      constexpr int kMaxRows = SPLIT ? 2 * ROWS : ROWS;
+      if (nrows > kMaxRows) {  // more ranks than the routing can reach: a layout of another routing
         if (lane == 0) set_error(p.error_word, EP_ERRBIT_STALE_LAYOUT);
-        if (pos >= ROWS) slot = -1;
-        nrows = ROWS;
+        if (pos >= kMaxRows) slot = -1;
+        nrows = kMaxRows;
       }
-      for (int c = 0; c < nchunk; ++c, ++i) {
-        const int s = static_cast<int>(i % kCombineStages);
+      const int parts = (SPLIT && nrows > ROWS) ? 2 : 1;
+      for (int c = 0; c < nchunk && ok; ++c) {
         const int elems = min(kChunk, p.H - c * kChunk);
-        unsigned char *stage = stages + (size_t)s * kStageBytes;
-        if (i >= kCombineStages) {
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], (uint32_t)(i / kCombineStages - 1) & 1u));
-          if (!ok) break;
+        for (int part = 0; part < parts; ++part, ++i) {
+          const int s = static_cast<int>(i % kCombineStages);
+          unsigned char *stage = stages + (size_t)s * kStageBytes;
+          if (i >= kCombineStages) {
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], (uint32_t)(i / kCombineStages - 1) & 1u));
+            if (!ok) break;
+          }
+          const int r0 = part * ROWS;
+          const int n = min(nrows - r0, ROWS);
+          const bool mine = slot >= 0 && pos >= r0 && pos < r0 + n;
+          int *hdr = reinterpret_cast<int *>(stage);
+          float *hdr_coef = reinterpret_cast<float *>(stage + 16);
+          if (mine) hdr_coef[pos - r0] = coef;
+          if (lane == 0) {
+            hdr[0] = n;
+            hdr[1] = t;
+            hdr[2] = t_next;
+            hdr[3] = part + 1 < parts ? 1 : 0;  // the sum goes on in the next unit
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)n * (uint32_t)elems * 2u);
+          __syncwarp();
+          if (mine)
+            bulk_load(stage + kStageHeader + (size_t)(pos - r0) * kChunkBytes,
+                      p.y + (size_t)slot * p.H + (size_t)c * kChunk, (uint32_t)elems * 2u, &full[s]);
+          if (lane == 0) loads_issued = i + 1;
         }
-        int *hdr = reinterpret_cast<int *>(stage);
-        float *hdr_coef = reinterpret_cast<float *>(stage + 16);
-        if (slot >= 0) hdr_coef[pos] = coef;
-        if (lane == 0) {
-          hdr[0] = nrows;
-          hdr[1] = t;
-          hdr[2] = t_next;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)nrows * (uint32_t)elems * 2u);
-        __syncwarp();
-        if (slot >= 0)
-          bulk_load(stage + kStageHeader + (size_t)pos * kChunkBytes,
-                    p.y + (size_t)slot * p.H + (size_t)c * kChunk, (uint32_t)elems * 2u, &full[s]);
-        if (lane == 0) loads_issued = i + 1;
       }
       t = t_next;
       cur = nxt;
@@ -413,7 +425,7 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
     bool more = true;
     while (more && !*s_abort) {
       for (int c = 0; c < nchunk; ++c, ++i) {
-        const int s = static_cast<int>(i % kCombineStages);
+        int s = static_cast<int>(i % kCombineStages);
         const int cols = min(kChunk, p.H - c * kChunk) / 8;
         const unsigned char *stage = stages + (size_t)s * kStageBytes;
         // a unit has at most one column per reducer thread: its bias loads
@@ -454,21 +466,49 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
         const float *hdr_coef = reinterpret_cast<const float *>(stage + 16);
         uint16_t *out = p.out + (size_t)t * p.H + (size_t)c * kChunk;
         static_assert(kChunk / 8 <= kReducers * kWarpSize, "one column per reducer thread");
+        float acc[8];
         if (rt < cols) {
-          const int col = rt;
-          float acc[8];
           seed(acc, p, b0, b1);
           for (int r = 0; r < nrows; ++r) {
             const int4 v =
-                *reinterpret_cast<const int4 *>(stage + kStageHeader + (size_t)r * kChunkBytes + col * 16);
+                *reinterpret_cast<const int4 *>(stage + kStageHeader + (size_t)r * kChunkBytes + rt * 16);
             accumulate<WEIGHTED, true>(acc, v, hdr_coef[r]);
           }
+        }
+        // a continuation: the token's remaining rows of this chunk, summed on
+        for (int carry = SPLIT ? hdr[3] : 0; carry != 0 && more;) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+          ++i;
+          s = static_cast<int>(i % kCombineStages);
+          stage = stages + (size_t)s * kStageBytes;
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (uint32_t)(i / kCombineStages) & 1u))) {
+            if (lane == 0) {
+              *s_abort = 1;
+              set_error(p.error_word, EP_ERRBIT_TIMEOUT);
+            }
+            more = false;
+            break;
+          }
+          const int *h2 = reinterpret_cast<const int *>(stage);
+          const float *c2 = reinterpret_cast<const float *>(stage + 16);
+          if (rt < cols) {
+            for (int r = 0; r < h2[0]; ++r) {
+              const int4 v =
+                  *reinterpret_cast<const int4 *>(stage + kStageHeader + (size_t)r * kChunkBytes + rt * 16);
+              accumulate<WEIGHTED, true>(acc, v, c2[r]);
+            }
+          }
+          carry = h2[3];
+        }
+        if (!more) break;
+        if (rt < cols) {
           int4 o;
           o.x = (int)pack_bf16x2(acc[0], acc[1]);
           o.y = (int)pack_bf16x2(acc[2], acc[3]);
           o.z = (int)pack_bf16x2(acc[4], acc[5]);
           o.w = (int)pack_bf16x2(acc[6], acc[7]);
-          st_stream_v4(out + (size_t)col * 8, o);
+          st_stream_v4(out + (size_t)rt * 8, o);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -486,11 +526,11 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
   }
 }
 
-template <bool WEIGHTED, int ROWS>
+template <bool WEIGHTED, int ROWS, bool SPLIT>
 ep_status_t launch_ws_rows(const CombineParams &p, const DeviceInfo &di, cudaStream_t stream) {
   static std::mutex mu;
   static bool configured[64] = {};
-  const auto kernel = combine_ws_kernel<WEIGHTED, ROWS>;
+  const auto kernel = combine_ws_kernel<WEIGHTED, ROWS, SPLIT>;
   const size_t smem = 128 + (size_t)kCombineStages * (kStageHeader + (size_t)ROWS * kChunkBytes);
   {
     std::lock_guard<std::mutex> g(mu);
@@ -510,15 +550,19 @@ ep_status_t launch_ws_rows(const CombineParams &p, const DeviceInfo &di, cudaStr
   return EP_OK;
 }
 
-// A token has at most min(K, R) rank rows under a given routing: with at
-// most 6, stages of 6 rows (four blocks per SM instead of three).
+// A token has at most min(K, R) rank rows under a given routing.  With at
+// most 6, stages of 6 rows (four blocks per SM instead of three).  With more
+// and many tokens, also 6-row stages, the wider tokens split in two units:
+// measured faster at 65 536 tokens (the occupancy), slower at 8192 (the
+// split units), so only from kSplitMinTokens on.
 template <bool WEIGHTED>
 ep_status_t launch_ws(const CombineParams &p, const DeviceInfo &di, cudaStream_t stream) {
   if constexpr (WEIGHTED) {
     if (!p.expanded && std::min(p.K, p.D) <= kSmallStageRows)
-      return launch_ws_rows<WEIGHTED, kSmallStageRows>(p, di, stream);
+      return launch_ws_rows<WEIGHTED, kSmallStageRows, false>(p, di, stream);
+    if (!p.expanded && p.T >= kSplitMinTokens) return launch_ws_rows<WEIGHTED, kSmallStageRows, true>(p, di, stream);
   }
-  return launch_ws_rows<WEIGHTED, kWsMaxRanks>(p, di, stream);
+  return launch_ws_rows<WEIGHTED, kWsMaxRanks, false>(p, di, stream);
 }
 
 constexpr bool kUseWsCombine = true;

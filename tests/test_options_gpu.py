@@ -110,3 +110,30 @@ def test_combine_bias(R, E, biases, weighted):
     assert np.array_equal(g, o)
     if b0 is not None and b1 is None:
         assert np.array_equal(g[:20], b0[:20])
+
+
+def test_combine_many_tokens_wide_routing():
+    """33 000 tokens of a top-8 routing over 8 ranks: the combine takes the
+    many-token configuration, whose stages hold 6 rows, so a token on 7 or
+    8 ranks is summed over two units per chunk (the biases seed only the
+    first).  Every output against the oracle, bit for bit."""
+    biases = ("b0", "b1")
+    T, H, K, E, R = 33_000, 2048 + 64, 8, 64, 8
+    idx, w, rng = _routing(T, K, E, 13, p_mask=0.05)
+    epr = E // R
+    fan = np.array([len(set((row // epr).tolist())) for row in idx])
+    assert (fan > 6).sum() > 1000
+    b0 = W.normal_bf16(rng, (T, H)) if "b0" in biases else None
+    b1 = W.normal_bf16(rng, (T, H)) if "b1" in biases else None
+    lay_o = oracle.get_layout(idx, E, R)
+    N = int(lay_o["rank_prefix"][R])
+    y = W.normal_bf16(rng, (N, H))
+    o, _ = oracle.combine(y, lay_o["token_slot"], idx, w, E, bias0=b0, bias1=b1)
+    idx_d = torch.from_numpy(idx).to(U.dev())
+    lay = ep.ep_get_layout(idx_d, E, R)
+    out = ep.ep_combine(U.to_dev_bf16(y), lay, idx_d, torch.from_numpy(w).to(U.dev()),
+                        bias0=None if b0 is None else U.to_dev_bf16(b0),
+                        bias1=None if b1 is None else U.to_dev_bf16(b1))
+    torch.cuda.synchronize()
+    assert lay.errors() == 0
+    U.assert_combine_exact(U.bits(out), o)
