@@ -251,7 +251,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
 //                     column per thread (fp32, separate multiply and add),
 //                     store the bf16 result and release the stage.
 // The loader runs `stages` units ahead, so the memory pipe does not wait on
-// the per-token metadata or on the reduction.
+// the per-token metadata or on the reduction.  A stage holds ROWS rows; with
+// SPLIT, a token with more rows sends each chunk as two units, the second
+// header flagged, and the reducers carry the partial sum from the first in
+// registers (rows stay in ascending rank order, so the sum is unchanged).
 
 constexpr int kWsMaxRanks = 8;
 constexpr int kSmallStageRows = 6;
@@ -265,7 +268,7 @@ constexpr int kChunkBytes = kChunk * 2;
 constexpr int kReducers = 8;                   // warps
 constexpr int kWsCombineThreads = (1 + kReducers) * kWarpSize;
 constexpr int kCombineStages = 2;
-constexpr int kStageHeader = 128;              // n, coefficients
+constexpr int kStageHeader = 128;              // n, token, next token, carry flag; coefficients from 16
 
 // One token's routing as the loader warp holds it: lane r < R has the slot
 // of rank r, lane k < K the k-th expert id and gate weight.
