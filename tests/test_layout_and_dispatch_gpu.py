@@ -142,6 +142,16 @@ def test_many_tokens_few_columns():
     _check(x, idx, w, E, R, "fp8", rows=np.sort(np.random.default_rng(0).choice(400_000, 3000, replace=False)))
 
 
+def test_largest_one_launch_layout():
+    """2048 blocks of 256 tokens, the most the one-launch layout takes: its
+    last block scans every block's totals.  The whole layout and a sample
+    of the rows against the oracle."""
+    T, H, K, E, R = 2048 * 256, 128, 4, 32, 8
+    idx, w, rng = _routing(T, K, E, 14)
+    x = W.normal_bf16(rng, (T, H))
+    _check(x, idx, w, E, R, "fp8", rows=np.sort(np.random.default_rng(3).choice(T, 3000, replace=False)))
+
+
 def test_more_tokens_than_the_one_launch_layout_takes():
     """Past 2048 blocks of 256 tokens the call lays out with both layout
     kernels first; the results are the same."""
