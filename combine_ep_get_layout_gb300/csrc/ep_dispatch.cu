@@ -503,9 +503,10 @@ __device__ __forceinline__ void dispatch_ws_body(const DispatchParams &p) {
       const float w = (lane < p.K && p.recv_topk_weights != nullptr)
                           ? __ldg(p.topk_weights + (size_t)t * p.K + lane) : 0.0f;
       // local layout: the block's bases, loaded alongside the slots
-      const int32_t *blk = p.local_base + (size_t)(t / kLocalTokensPerBlock) * p.R;
-      const int base_lo = (p.local_base != nullptr && lane < p.D) ? __ldg(blk + lane) : 0;
-      const int base_hi = (p.local_base != nullptr && lane + kWarpSize < p.D) ? __ldg(blk + lane + kWarpSize) : 0;
+      const size_t blk = (size_t)(t / kLocalTokensPerBlock) * p.R;
+      const int base_lo = (p.local_base != nullptr && lane < p.D) ? __ldg(p.local_base + blk + lane) : 0;
+      const int base_hi = (p.local_base != nullptr && lane + kWarpSize < p.D)
+                              ? __ldg(p.local_base + blk + lane + kWarpSize) : 0;
       if (p.local_base != nullptr) {
         // finish the layout of token t: absolute slots, written back; its
         // experts counted; ids outside [-1, E) flagged
