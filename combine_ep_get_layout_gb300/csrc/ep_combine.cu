@@ -363,8 +363,14 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
         }
         break;
       }
-      const int t_next = draw(j);
-      const TokenMeta nxt = t_next >= 0 ? fetch_meta(p, t_next, lane, WEIGHTED) : cur;  // in flight meanwhile
+      // With more than two chunks a token, the next token is drawn once this
+      // token's first unit is issued: a block's first loads then wait for
+      // one ticket, not two, and only the token's last unit names it.  With
+      // one or two chunks the ticket and the metadata would have a single
+      // unit to arrive in (measured slower), so they are drawn before it.
+      const bool late = nchunk > 2;
+      int t_next = late ? -1 : draw(j);
+      TokenMeta nxt = t_next >= 0 ? fetch_meta(p, t_next, lane, WEIGHTED) : cur;  // in flight meanwhile
       int slot = cur.slot;
       if (WEIGHTED && !layout_agrees(p, cur.e, slot, -1, lane) && lane == 0)
         set_error(p.error_word, EP_ERRBIT_STALE_LAYOUT);
@@ -411,6 +417,10 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
             bulk_load(stage + kStageHeader + (size_t)(pos - r0) * kChunkBytes,
                       p.y + (size_t)slot * p.H + (size_t)c * kChunk, (uint32_t)elems * 2u, &full[s]);
           if (lane == 0) loads_issued = i + 1;
+        }
+        if (late && c == 0 && ok) {
+          t_next = draw(j);
+          if (t_next >= 0) nxt = fetch_meta(p, t_next, lane, WEIGHTED);
         }
       }
       t = t_next;

@@ -147,6 +147,7 @@ COMBINE = [
     (2000, 2560, 6, 64, False, True),
     (1000, 1024, 16, 64, True, True),     # register combine (K > 8)
     (8192, 7168, 8, 256, True, False),
+    (1500, 6152, 6, 64, False, True),      # four chunks a row, the last of 8 elements
 ]
 
 

@@ -143,6 +143,10 @@ EDGE = [
     ("all_masked", 300, 256, 4, 16, 4, False, dict(p_mask=1.0)),
     ("half_masked", 2000, 256, 8, 64, 8, True, dict(p_mask=0.5)),
     ("plain_combine", 1500, 1024, 6, 64, 8, False, dict(weighted=False)),
+    # rows of three full chunks and an 8-element tail: the combine draws a
+    # block's next token after the first chunk
+    ("plain_combine_four_chunks", 700, 6152, 6, 64, 8, False, dict(weighted=False)),
+    ("weighted_combine_four_chunks", 700, 6152, 6, 64, 8, False, {}),
 ]
 
 
