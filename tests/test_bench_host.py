@@ -1,5 +1,5 @@
-"""Host-side logic of bench.py, CPU only: algorithmic byte counts, the
-ncu-traffic lookup, and the multi-replica aggregation (maximum over ranks,
+"""Host-side logic of bench.py, CPU only: algorithmic byte counts, the L2
+note, the ncu-traffic lookup, and the multi-replica aggregation (maximum over ranks,
 barriers) with two gloo ranks on 127.0.0.1."""
 import os
 import socket
@@ -24,6 +24,18 @@ def test_algorithmic_bytes_headline():
     assert abs(b["combine"] / 1e6 - 741) < 2
     bf = bench.algorithmic_bytes(W.CONFIGS["bf16_4096x4096_top6_64e"], N=18477)
     assert bf["dispatch"] > 4096 * 4096 * 2 + 18477 * 4096 * 2
+
+
+def test_l2_note_says_which_timing_rule_holds():
+    """No L2 flush is done between steps, so a line is a bandwidth figure
+    only when a step moves well over the L2's 129 MB; a workload that fits
+    says so."""
+    head = bench.config_dict(W.CONFIGS["fp8_8192x7168_top8_256e"], 43206)["l2"]
+    assert head.startswith("inputs larger than L2") and "1.18 GB" in head
+    bf = bench.l2_note(W.CONFIGS["bf16_4096x4096_top6_64e"], 18624)
+    assert bf.startswith("inputs larger than L2")
+    tiny = bench.l2_note(W.CONFIGS["tiny_128x256_top2_16e"], 229)
+    assert tiny.startswith("fits in L2") and "launch-bound" in tiny
 
 
 def test_traffic_lookup_needs_matching_source(tmp_path, monkeypatch):
