@@ -93,3 +93,28 @@ def test_reference_arm_other_ranks_exit_without_work():
         steps = 1
         warmup = 3
     assert bench.run_reference(A, rank=1, world=2) == 0
+
+
+def test_reference_arm_line_on_the_tiny_workload(capsys):
+    """Rank 0 of `--impl reference` prints one JSON line with the GPU arm's
+    metric, unit, direction and config (received rows included), a
+    cpu_baseline describing the run and an e2e that moves no bytes."""
+    import json
+
+    class A:
+        workload = "tiny_128x256_top2_16e"
+        steps = 2
+        warmup = 3
+    assert bench.run_reference(A, rank=0, world=1) == 0
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    cfg = W.CONFIGS[A.workload]
+    assert line["impl"] == "reference"
+    assert (line["metric"], line["unit"], line["higher_is_better"]) == (bench.METRIC, bench.UNIT, False)
+    assert line["config"] == bench.config_dict(cfg, 229)  # the tiny workload: 229 received rows
+    assert line["value"] > 0 and line["steps"] == 2 and line["warmup"] == 3
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": bench.UNIT,
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
