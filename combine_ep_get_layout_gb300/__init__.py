@@ -52,6 +52,14 @@ def _check(status: int, fn: str):
         raise EPError(status, f"{fn}: {name}: {detail}")
 
 
+def _call(dev: torch.device, fn: str, *args):
+    """Calls the library function ``fn`` with ``dev`` as the current CUDA
+    device: the library launches on the calling thread's current device,
+    which must be the one holding the tensors and owning the stream."""
+    with torch.cuda.device(dev):
+        _check(getattr(N.load(), fn)(*args), fn)
+
+
 def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else C.c_void_p(t.data_ptr())
 
@@ -144,9 +152,9 @@ def ep_get_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int,
     elif (layout.num_tokens, layout.num_experts, layout.num_ranks) != (T, num_experts, num_ranks):
         raise ValueError("layout was allocated for other sizes")
     st = layout.c_struct()
-    _check(N.load().ep_get_layout(
-        _ptr(topk_idx), T, K, num_experts, num_ranks, C.byref(st),
-        _ptr(layout.workspace), layout.workspace.numel(), _stream(stream, dev)), "ep_get_layout")
+    _call(dev, "ep_get_layout",
+          _ptr(topk_idx), T, K, num_experts, num_ranks, C.byref(st),
+          _ptr(layout.workspace), layout.workspace.numel(), _stream(stream, dev))
     return layout
 
 
@@ -162,9 +170,9 @@ def ep_get_layout_noalloc(topk_idx: torch.Tensor, num_experts: int, num_ranks: i
     if (layout.num_tokens, layout.num_experts, layout.num_ranks) != (T, num_experts, num_ranks):
         raise ValueError("layout was allocated for other sizes")
     st = layout.c_struct()
-    _check(N.load().ep_get_layout_noalloc(
-        _ptr(topk_idx), T, K, num_experts, num_ranks, C.byref(st),
-        _stream(stream, topk_idx.device)), "ep_get_layout_noalloc")
+    _call(topk_idx.device, "ep_get_layout_noalloc",
+          _ptr(topk_idx), T, K, num_experts, num_ranks, C.byref(st),
+          _stream(stream, topk_idx.device))
     return layout
 
 
@@ -256,17 +264,16 @@ def ep_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: Optional[
     T, H = x.shape
     K = topk_idx.shape[1]
     st = layout.c_struct()
-    lib = N.load()
     if code == N.EP_DTYPE_FP8_E4M3_PACKED or cumulative_recv_stats is not None:
         args = _dispatch_args(x, topk_idx, topk_weights, E, R, st, code, out, recv_capacity,
                               cumulative_recv_stats)
-        _check(lib.ep_dispatch_ex(C.byref(args), _stream(stream, dev)), "ep_dispatch_ex")
+        _call(dev, "ep_dispatch_ex", C.byref(args), _stream(stream, dev))
     else:
-        _check(lib.ep_dispatch(
-            _ptr(x), T, H, _ptr(topk_idx), _ptr(topk_weights), K, E, R, C.byref(st), code,
-            _ptr(out.recv_x), _ptr(out.recv_x_scales), _ptr(out.recv_src_idx),
-            _ptr(out.recv_topk_idx), _ptr(out.recv_topk_weights), recv_capacity,
-            _stream(stream, dev)), "ep_dispatch")
+        _call(dev, "ep_dispatch",
+              _ptr(x), T, H, _ptr(topk_idx), _ptr(topk_weights), K, E, R, C.byref(st), code,
+              _ptr(out.recv_x), _ptr(out.recv_x_scales), _ptr(out.recv_src_idx),
+              _ptr(out.recv_topk_idx), _ptr(out.recv_topk_weights), recv_capacity,
+              _stream(stream, dev))
     return out
 
 
@@ -292,9 +299,8 @@ def ep_get_layout_and_dispatch(x: torch.Tensor, topk_idx: torch.Tensor,
     st = layout.c_struct()
     args = _dispatch_args(x, topk_idx, topk_weights, num_experts, num_ranks, st, code, out,
                           recv_capacity, cumulative_recv_stats)
-    _check(N.load().ep_get_layout_and_dispatch(
-        C.byref(args), _ptr(layout.workspace), layout.workspace.numel(), _stream(stream, dev)),
-        "ep_get_layout_and_dispatch")
+    _call(dev, "ep_get_layout_and_dispatch",
+          C.byref(args), _ptr(layout.workspace), layout.workspace.numel(), _stream(stream, dev))
     return layout, out
 
 
@@ -332,7 +338,6 @@ def ep_combine(y: torch.Tensor, layout: Layout, topk_idx: Optional[torch.Tensor]
         out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     _want(out, "out", torch.bfloat16, dev)
     st = layout.c_struct()
-    lib = N.load()
     if bias0 is not None or bias1 is not None:
         args = N.ep_combine_args_t(
             y.data_ptr(), cap, H, C.pointer(st), T, R,
@@ -340,11 +345,11 @@ def ep_combine(y: torch.Tensor, layout: Layout, topk_idx: Optional[torch.Tensor]
             None if topk_weights is None else topk_weights.data_ptr(), K, layout.num_experts,
             None if bias0 is None else bias0.data_ptr(),
             None if bias1 is None else bias1.data_ptr(), out.data_ptr())
-        _check(lib.ep_combine_ex(C.byref(args), _stream(stream, dev)), "ep_combine_ex")
+        _call(dev, "ep_combine_ex", C.byref(args), _stream(stream, dev))
     else:
-        _check(lib.ep_combine(
-            _ptr(y), cap, H, C.byref(st), T, R, _ptr(topk_idx), _ptr(topk_weights), K,
-            layout.num_experts, _ptr(out), _stream(stream, dev)), "ep_combine")
+        _call(dev, "ep_combine",
+              _ptr(y), cap, H, C.byref(st), T, R, _ptr(topk_idx), _ptr(topk_weights), K,
+              layout.num_experts, _ptr(out), _stream(stream, dev))
     return out
 
 
@@ -414,9 +419,9 @@ def ep_get_layout_expanded(topk_idx: torch.Tensor, num_experts: int, expert_alig
         raise ValueError("layout was allocated for other sizes")
     layout.expert_alignment = expert_alignment
     st = layout.c_struct()
-    _check(N.load().ep_get_layout_expanded(
-        _ptr(topk_idx), T, K, num_experts, expert_alignment, C.byref(st), _ptr(layout.workspace),
-        layout.workspace.numel(), _stream(stream, dev)), "ep_get_layout_expanded")
+    _call(dev, "ep_get_layout_expanded",
+          _ptr(topk_idx), T, K, num_experts, expert_alignment, C.byref(st), _ptr(layout.workspace),
+          layout.workspace.numel(), _stream(stream, dev))
     return layout
 
 
@@ -466,7 +471,7 @@ def ep_dispatch_expanded(x: torch.Tensor, topk_idx: torch.Tensor,
         None if out.recv_topk_weights is None else out.recv_topk_weights.data_ptr(),
         recv_capacity, 1 if zero_padding else 0,
         None if cumulative_recv_stats is None else cumulative_recv_stats.data_ptr())
-    _check(N.load().ep_dispatch_expanded(C.byref(args), _stream(stream, dev)), "ep_dispatch_expanded")
+    _call(dev, "ep_dispatch_expanded", C.byref(args), _stream(stream, dev))
     return out
 
 
@@ -494,5 +499,5 @@ def ep_combine_expanded(y: torch.Tensor, layout: ExpandedLayout,
         None if topk_weights is None else topk_weights.data_ptr(), layout.num_experts,
         None if bias0 is None else bias0.data_ptr(), None if bias1 is None else bias1.data_ptr(),
         out.data_ptr())
-    _check(N.load().ep_combine_expanded(C.byref(args), _stream(stream, dev)), "ep_combine_expanded")
+    _call(dev, "ep_combine_expanded", C.byref(args), _stream(stream, dev))
     return out

@@ -19,7 +19,9 @@
  *     the device or the stream, and keeps no state between calls beyond
  *     per-device launch parameters (SM count, occupancy) cached on first use.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
- *     legacy default stream).
+ *     legacy default stream).  Kernels launch on the calling thread's
+ *     current CUDA device (cudaSetDevice): every pointer must be that
+ *     device's memory and `stream` must belong to it.
  *   - Sizes: T tokens, K top-k slots, E experts, R logical ranks, H hidden,
  *     N = number of dispatched rows = sum of per-rank token counts.
  *     Expert e belongs to rank floor(e / (E/R)); E % R must be 0.
