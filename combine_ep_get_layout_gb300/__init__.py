@@ -65,8 +65,13 @@ def _ptr(t: Optional[torch.Tensor]):
 
 
 def _stream(stream, device) -> C.c_void_p:
-    s = torch.cuda.current_stream(device) if stream is None else stream
-    return C.c_void_p(s.cuda_stream)
+    """The handle of ``stream`` (default: the device's current stream), which
+    must belong to the tensors' device."""
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    elif stream.device != device:
+        raise ValueError(f"stream is on {stream.device}, the tensors on {device}")
+    return C.c_void_p(stream.cuda_stream)
 
 
 def _want(t: torch.Tensor, name: str, dtype, device=None):

@@ -91,3 +91,12 @@ def test_every_launch_runs_with_the_tensors_device_current(lib):
     assert all(d == x.device for _, d in launched), launched
     # the size queries need no device
     assert all(n not in LAUNCHING for n, d in lib.calls if d is None)
+
+
+def test_a_stream_of_another_device_is_rejected():
+    class Stream:  # the attributes the binding reads from a torch.cuda.Stream
+        def __init__(self, device, handle):
+            self.device, self.cuda_stream = torch.device(device), handle
+    assert ep._stream(Stream("cuda:0", 1234), torch.device("cuda:0")).value == 1234
+    with pytest.raises(ValueError, match="stream is on cuda:1"):
+        ep._stream(Stream("cuda:1", 1234), torch.device("cuda:0"))
