@@ -376,6 +376,15 @@ def test_every_token_on_every_rank(fp8):
     U.assert_layout_equal(g["layout"], lay_o)
     U.assert_dispatch_equal(g, d_o, N, fp8)
     U.assert_combine_exact(g["combined"], c_o)
+    # the same through the one call (one-launch layout, slots finished by the dispatch)
+    lay2, d2 = ep.ep_get_layout_and_dispatch(
+        U.to_dev_bf16(x), torch.from_numpy(idx).to(U.dev()), torch.from_numpy(w).to(U.dev()), E, R,
+        dtype="fp8" if fp8 else "bf16", recv_capacity=N)
+    torch.cuda.synchronize()
+    U.assert_layout_equal(U.layout_np(lay2), lay_o)
+    g2 = {k: None if getattr(d2, k) is None else U.bits(getattr(d2, k))
+          for k in ("recv_x", "recv_x_scales", "recv_src_idx", "recv_topk_idx", "recv_topk_weights")}
+    U.assert_dispatch_equal(g2, d_o, N, fp8)
 
 
 def test_combine_every_token_split():
