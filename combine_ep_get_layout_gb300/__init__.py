@@ -30,7 +30,8 @@ __all__ = ["EPError", "Layout", "Dispatched", "ep_layout_workspace_bytes",
            "ep_get_layout_and_dispatch",
            "ep_combine", "ep_combine_ex", "ep_fp8_packed_row_bytes", "ExpandedLayout",
            "ep_expanded_layout_workspace_bytes", "ep_get_layout_expanded",
-           "ep_dispatch_expanded", "ep_combine_expanded", "library_path"]
+           "ep_dispatch_expanded", "ep_combine_expanded", "ep_selftest_bounded_waits",
+           "library_path"]
 
 
 class EPError(RuntimeError):
@@ -506,3 +507,21 @@ def ep_combine_expanded(y: torch.Tensor, layout: ExpandedLayout,
         out.data_ptr())
     _call(dev, "ep_combine_expanded", C.byref(args), _stream(stream, dev))
     return out
+
+
+def ep_selftest_bounded_waits(device=None, stream=None) -> dict:
+    """The library's self-test of its bounded device waits (about one second
+    of GPU time): an mbarrier wait that nothing completes and a grid barrier
+    that one block never reaches must both give up after the wait limit.
+    Waits for the stream, then returns ``{"gave_up": [mbarrier, grid barrier],
+    "elapsed_ns": [...], "error_word": ...}``."""
+    dev = torch.device("cuda" if device is None else device)
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    gave_up = torch.full((2,), -1, dtype=torch.int32, device=dev)
+    elapsed = torch.zeros(2, dtype=torch.int64, device=dev)
+    _call(dev, "ep_selftest_bounded_waits", _ptr(err), _ptr(gave_up), _ptr(elapsed), _stream(stream, dev))
+    (torch.cuda.current_stream(dev) if stream is None else stream).synchronize()
+    return {"gave_up": gave_up.tolist(), "elapsed_ns": elapsed.tolist(),
+            "error_word": int(err.item()) & 0xffffffff}

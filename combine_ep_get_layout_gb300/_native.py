@@ -122,6 +122,7 @@ SIGNATURES = {
     "ep_get_layout_expanded": (_i, [_p, _i, _i, _i, _i, C.POINTER(ep_expanded_layout_t), _p, _sz, _p]),
     "ep_dispatch_expanded": (_i, [C.POINTER(ep_dispatch_expanded_args_t), _p]),
     "ep_combine_expanded": (_i, [C.POINTER(ep_combine_expanded_args_t), _p]),
+    "ep_selftest_bounded_waits": (_i, [_p, _p, _p, _p]),
     "ep_status_str": (C.c_char_p, [_i]),
     "ep_last_error": (C.c_char_p, []),
     "ep_abi_version": (_i, []),

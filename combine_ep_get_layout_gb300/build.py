@@ -23,7 +23,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libep_gb300.so")
 
 SOURCES = ["ep_api.cu", "ep_layout.cu", "ep_layout_expanded.cu", "ep_dispatch.cu", "ep_combine.cu",
-           "ep_noalloc.cu"]
+           "ep_noalloc.cu", "ep_selftest.cu"]
 HEADERS = ["ep_device.cuh", "ep_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",

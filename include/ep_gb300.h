@@ -478,6 +478,27 @@ typedef struct {
 } ep_combine_expanded_args_t;
 ep_status_t ep_combine_expanded(const ep_combine_expanded_args_t *args, ep_stream_t stream);
 
+/*
+ * Self-test of the bounded device waits (the pages have no counterpart: the
+ * library's own guarantee that a data or hand-over problem never hangs the
+ * GPU).  Launches two blocks of 32 threads on `stream`: block 0 waits on an
+ * mbarrier that nothing arrives on, the form of the dispatch and combine
+ * stage waits; block 1 enters a grid barrier that block 0 never reaches, the
+ * form of the expanded layout's barrier.  Each wait gives up after the
+ * library's wait limit (1 s of the GPU's global timer), and the kernel
+ * returns.
+ *   error_word  [1] uint32: EP_ERRBIT_TIMEOUT is OR-ed in by a wait that gave up
+ *   gave_up     [2] int32 : 1 where wait i (0: mbarrier, 1: grid barrier)
+ *                           gave up, 0 where it completed
+ *   elapsed_ns  [2] uint64: the time each wait took, from the global timer
+ * Device pointers, caller-owned, 4-, 4- and 8-byte aligned; NULL or
+ * misaligned gives EP_ERR_INVALID_ARG.  Takes about one second of GPU time;
+ * calls must not overlap on the GPU (the grid barrier's words are a static
+ * device variable).
+ */
+ep_status_t ep_selftest_bounded_waits(uint32_t *error_word, int32_t *gave_up, uint64_t *elapsed_ns,
+                                      ep_stream_t stream);
+
 /* A static, human-readable name of a status. */
 const char *ep_status_str(ep_status_t status);
 

@@ -343,3 +343,15 @@ def test_layout_and_dispatch_rejects(lib):
     name, msg = _status(lib, lib.ep_get_layout_and_dispatch(C.byref(args2), FAKE, need, None))
     assert name == "EP_ERR_INVALID_ARG" and "hidden" in msg
     assert _status(lib, lib.ep_get_layout_and_dispatch(None, FAKE, need, None))[0] == "EP_ERR_INVALID_ARG"
+
+
+def test_selftest_bounded_waits_rejects(lib):
+    """The wait self-test checks its three output pointers on the host, before
+    any CUDA call."""
+    f = lib.ep_selftest_bounded_waits
+    name, msg = _status(lib, f(None, FAKE, FAKE, None))
+    assert name == "EP_ERR_INVALID_ARG" and "error_word" in msg
+    name, msg = _status(lib, f(FAKE, None, FAKE, None))
+    assert name == "EP_ERR_INVALID_ARG" and "gave_up" in msg
+    name, msg = _status(lib, f(FAKE, FAKE, C.c_void_p(FAKE.value + 4), None))
+    assert name == "EP_ERR_INVALID_ARG" and "elapsed_ns" in msg
