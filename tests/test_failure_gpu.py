@@ -11,6 +11,7 @@ import oracle
 import workloads as W
 
 pytestmark = pytest.mark.gpu
+RUN_ORDER = 2  # last (see conftest.py)
 
 ep = pytest.importorskip("combine_ep_get_layout_gb300")
 

@@ -6,8 +6,9 @@ It uses the library's static scratch instead of a workspace.
 
 Called through the C ABI, on two calls in a row, its layout must equal the
 one ep_get_layout computes with a workspace (integer outputs: bit-exact).
-This file is collected last so that a failure here comes after every other
-test has run; it also passes on its own in a fresh process."""
+This file is collected after the other parity files (only files that set
+RUN_ORDER run later), so that a failure here comes after those have run; it
+also passes on its own in a fresh process."""
 import ctypes as C
 
 import numpy as np
