@@ -355,3 +355,39 @@ def test_selftest_bounded_waits_rejects(lib):
     assert name == "EP_ERR_INVALID_ARG" and "gave_up" in msg
     name, msg = _status(lib, f(FAKE, FAKE, C.c_void_p(FAKE.value + 4), None))
     assert name == "EP_ERR_INVALID_ARG" and "elapsed_ns" in msg
+
+
+C_CONSUMER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "ep_gb300.h"
+int main(void) {
+  if (ep_abi_version() != EP_ABI_VERSION) return 1;
+  size_t ws = ep_layout_workspace_bytes(8192, 256, 8);
+  ep_status_t s = ep_get_layout(NULL, 8192, 8, 256, 8, NULL, NULL, 0, NULL);
+  printf("%zu %s %d\n", ws, ep_status_str(s), (int)(strlen(ep_last_error()) > 0));
+  return s == EP_ERR_INVALID_ARG ? 0 : 2;
+}
+"""
+
+
+def test_a_c99_program_links_and_calls_the_library(lib, tmp_path):
+    """The boundary is plain C: a strict C99 program includes the header,
+    links the library and calls its host-side entry points (no GPU needed
+    for these)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    from combine_ep_get_layout_gb300 import _native
+    libdir = os.path.dirname(_native.LIB_PATH)
+    src = tmp_path / "consumer.c"
+    src.write_text(C_CONSUMER)
+    exe = tmp_path / "consumer"
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I", os.path.join(ROOT, "include"), str(src), "-L", libdir, "-lep_gb300",
+                    f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    # 256 header bytes + one int32 total per (256-token block, rank)
+    assert out == [str(256 + (8192 // 256) * 8 * 4), "EP_ERR_INVALID_ARG", "1"]
