@@ -22,9 +22,9 @@ bool g_dev_ready[kMaxDevices] = {};
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-void clear_error() { g_last_error[0] = '\0'; }
-
 }  // namespace
+
+void clear_error() { g_last_error[0] = '\0'; }
 
 ep_status_t fail(ep_status_t status, const char *fmt, ...) {
   va_list ap;
@@ -77,8 +77,6 @@ const DeviceInfo *current_device_info() {
   return &g_dev[dev];
 }
 
-namespace {
-
 ep_status_t check_routing_sizes(const char *fn, int num_topk, int num_experts, int num_ranks) {
   if (num_topk < 1 || num_topk > EP_MAX_TOPK)
     return fail(num_topk < 1 ? EP_ERR_INVALID_ARG : EP_ERR_UNSUPPORTED, "%s: num_topk=%d not in [1, %d]", fn,
@@ -103,6 +101,8 @@ ep_status_t check_ptr(const char *fn, const char *name, const void *p, size_t al
   if (!aligned(p, align)) return fail(EP_ERR_INVALID_ARG, "%s: %s is not %zu-byte aligned", fn, name, align);
   return EP_OK;
 }
+
+namespace {
 
 #define EP_CHECK(expr)                   \
   do {                                   \

@@ -31,9 +31,20 @@ const DeviceInfo *current_device_info();
 // Record a detail message for ep_last_error() and return the status.
 ep_status_t fail(ep_status_t status, const char *fmt, ...);
 ep_status_t cuda_fail(cudaError_t err, const char *what);
+// Empty the calling thread's detail message (every entry point does first).
+void clear_error();
+
+// Host-side argument checks shared by the entry points: K, E and R within
+// the limits with E % R == 0; a pointer non-null when `required` and aligned
+// to `align` bytes when given.
+ep_status_t check_routing_sizes(const char *fn, int num_topk, int num_experts, int num_ranks);
+ep_status_t check_ptr(const char *fn, const char *name, const void *p, size_t align, bool required);
 
 // ---- layout (ep_layout.cu)
 size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
+// The bytes of the workspace that launch_layout touches (its grid is capped,
+// so at most this much of a larger workspace is used).
+size_t layout_workspace_bytes_used(int num_tokens, int num_ranks);
 ep_status_t launch_layout(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
                           int num_ranks, const ep_layout_t &layout, void *workspace,
                           cudaStream_t stream);

@@ -389,6 +389,12 @@ size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks) {
   return kPartialOffset + ((partial + 255) / 256) * 256;
 }
 
+size_t layout_workspace_bytes_used(int num_tokens, int num_ranks) {
+  const int grid = std::min(max_layout_blocks(num_tokens), kMaxLayoutBlocks);
+  const size_t partial = (size_t)grid * (size_t)num_ranks * sizeof(int32_t);
+  return kPartialOffset + ((partial + 255) / 256) * 256;
+}
+
 ep_status_t launch_layout(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
                           int num_ranks, const ep_layout_t &layout, void *workspace,
                           cudaStream_t stream) {

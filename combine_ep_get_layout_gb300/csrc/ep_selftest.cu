@@ -41,8 +41,6 @@ __global__ void __launch_bounds__(kWarpSize)
   }
 }
 
-bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
 }  // namespace
 }  // namespace ep
 
@@ -50,12 +48,11 @@ extern "C" ep_status_t ep_selftest_bounded_waits(uint32_t *error_word, int32_t *
                                                  ep_stream_t stream) {
   using namespace ep;
   static const char *fn = "ep_selftest_bounded_waits";
-  if (error_word == nullptr || !aligned(error_word, 4))
-    return fail(EP_ERR_INVALID_ARG, "%s: error_word is NULL or not 4-byte aligned", fn);
-  if (gave_up == nullptr || !aligned(gave_up, 4))
-    return fail(EP_ERR_INVALID_ARG, "%s: gave_up is NULL or not 4-byte aligned", fn);
-  if (elapsed_ns == nullptr || !aligned(elapsed_ns, 8))
-    return fail(EP_ERR_INVALID_ARG, "%s: elapsed_ns is NULL or not 8-byte aligned", fn);
+  clear_error();
+  ep_status_t s = check_ptr(fn, "error_word", error_word, 4, true);
+  if (s == EP_OK) s = check_ptr(fn, "gave_up", gave_up, 4, true);
+  if (s == EP_OK) s = check_ptr(fn, "elapsed_ns", elapsed_ns, 8, true);
+  if (s != EP_OK) return s;
   if (current_device_info() == nullptr) return EP_ERR_CUDA;
   // A plain launch (no programmatic dependent launch): the kernel starts once
   // the work ahead of it on the stream has finished.

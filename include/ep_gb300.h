@@ -17,7 +17,10 @@
  *     caller, row-major, and must stay alive until the stream has passed the
  *     call.  The library allocates nothing, frees nothing, never synchronises
  *     the device or the stream, and keeps no state between calls beyond
- *     per-device launch parameters (SM count, occupancy) cached on first use.
+ *     per-device launch parameters (SM count, occupancy, kernel attributes)
+ *     set up on first use and kept for the life of the process; a
+ *     cudaDeviceReset discards the kernel attributes, so the library must
+ *     not be called on a device after it has been reset.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream).  Kernels launch on the calling thread's
  *     current CUDA device (cudaSetDevice): every pointer must be that
@@ -136,9 +139,10 @@ size_t ep_layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks)
 
 /*
  * Layout: the count phase and the count exchange of TileScale PR #68
- * (README section "Design"; commit message on do_expand: "phase 1 tallies
- * per destination, phase 2 turns tallies into a base, phase 3 adds a
- * locally-claimed slot"), on one GPU.  Two kernels, the boundary between
+ * (README section "Design"; commit message on do_expand, which splits the
+ * work into per-destination counting, a base per destination derived from
+ * the counts, and a slot claimed locally and added to that base), on one
+ * GPU.  Two kernels, the boundary between
  * them standing in for the count exchange: the first counts each block's
  * tokens per rank (warp ballots, one bit per (token, rank) however many
  * experts map there) and publishes per-rank block totals; the second
@@ -174,12 +178,18 @@ ep_status_t ep_get_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
  * the library holds until the process exits.  It calls no allocating
  * routine.  The caller still passes topk_idx and the layout outputs.
  *
- *   Limit: ep_layout_workspace_bytes(T, E, R) must not exceed
- *   EP_NOALLOC_SCRATCH_BYTES, else EP_ERR_UNSUPPORTED (for R = 8 that is
- *   T <= 2,095,104 tokens; for R = 64, T <= 261,888).
+ *   Limit: the layout kernels run at most 2048 thread blocks and keep
+ *   R four-byte totals per block after a 256-byte header, so a call uses
+ *   256 + 4 * R * min(ceil(T / 256), 2048) bytes (rounded up to 256) of
+ *   the scratch.  That must not exceed EP_NOALLOC_SCRATCH_BYTES, else
+ *   EP_ERR_UNSUPPORTED: any T fits for R <= 31; for R = 32 the limit is
+ *   T <= 523,776 tokens, for R = 64, T <= 261,888.
  *   Set-up: the first call on a device looks up the device address of the
- *   scratch array once (with that device current); make that first call
- *   before any stream capture.
+ *   scratch array once (with that device current) and keeps it for the
+ *   life of the process; make that first call before any stream capture.
+ *   Like the library's other per-device set-up (kernel attributes,
+ *   device properties), it does not survive a cudaDeviceReset of that
+ *   device: do not call the library on a device after resetting it.
  *   Every call clears the scratch it uses, on `stream`, before its kernel.
  *   One scratch per device is shared by every call: calls that overlap on
  *   the GPU (unordered streams) race on it and produce wrong layouts, so

@@ -325,6 +325,22 @@ def test_work_counters_must_be_16_byte_aligned(lib):
     assert name == "EP_ERR_INVALID_ARG" and "work_counters" in msg
 
 
+@pytest.mark.parametrize("T,R", [(261_889, 64), (523_777, 32)])
+def test_noalloc_refuses_beyond_its_scratch(lib, T, R):
+    """The no-allocation layout refuses, before any CUDA call, a size whose
+    per-block rank totals (4 bytes x R for each of at most 2048 blocks of 256
+    tokens, after a 256-byte header) overflow its static scratch; the smallest
+    refused sizes at R = 64 and R = 32.  The message names the scratch and is
+    replaced by the next call's outcome."""
+    lay = _layout()
+    s = lib.ep_get_layout_noalloc(FAKE, T, 4, 128, R, C.byref(lay), None)
+    name, msg = _status(lib, s)
+    assert name == "EP_ERR_UNSUPPORTED" and "static scratch" in msg, msg
+    s = lib.ep_get_layout_noalloc(FAKE, T, 0, 128, R, C.byref(lay), None)
+    name, msg = _status(lib, s)
+    assert name == "EP_ERR_INVALID_ARG" and "num_topk" in msg and "scratch" not in msg, msg
+
+
 def test_layout_and_dispatch_rejects(lib):
     """ep_get_layout_and_dispatch checks the arguments of both calls, and its
     workspace against ep_layout_workspace_bytes, before any launch."""
