@@ -67,11 +67,12 @@ KERNEL_SOURCES = {
     "combine": ["ep_combine.cu", "ep_device.cuh"],
 }
 def kernel_symbol(kernel: str, cfg: W.EPConfig) -> str:
-    """The library kernel(s) that run each call for this workload (the
-    layout is two kernels; the library picks the warp-specialised dispatch,
+    """The library kernel(s) that run each separately timed call for this
+    workload (ep_get_layout is two kernels; the library picks the
+    warp-specialised dispatch,
     with the fp8 cast or without it for bf16, and the warp-specialised
     combine for up to 8 ranks)."""
-    if kernel == "layout":
+    if kernel == "layout":  # ep_get_layout; the step's one call runs layout_local_kernel
         return "layout_count_kernel+layout_slot_kernel"
     if kernel == "dispatch":
         return "dispatch_ws_kernel" if cfg.fp8 else "dispatch_ws_bf16_kernel"
@@ -169,6 +170,67 @@ class ClockSampler:
                 "samples": len(rows), "samples_under_load": len(loaded)}
 
 
+class GpuProcessSampler:
+    """Which processes use the GPU's SMs while the bench runs: `nvidia-smi
+    pmon` (read only, one sample a second) over the whole run.  A process
+    other than this one with SM use marks the line (`foreign_sm_use`); the
+    numbers of such a run may be disturbed.  When the GPU reports process ids
+    of another namespace than this process's, this process cannot be told
+    apart by id: then more than one process with SM use counts as foreign."""
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.out = ""
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", "pmon", "-s", "u", "-d", "1"]
+        if self.gpu_index is not None:
+            cmd += ["-i", str(self.gpu_index)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(1.2)  # one more sample after the last GPU work
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    @staticmethod
+    def parse(text: str, my_pid: int) -> dict:
+        """pmon lines -> {pid: max SM %} of the processes that used the SMs."""
+        seen = {}
+        for line in (text or "").splitlines():
+            f = line.split()
+            if len(f) < 4 or line.lstrip().startswith("#") or not f[1].isdigit():
+                continue
+            sm = f[3]
+            if sm.isdigit() and int(sm) > 0:
+                seen[int(f[1])] = max(seen.get(int(f[1]), 0), int(sm))
+        return seen
+
+    @staticmethod
+    def judge(seen: dict, my_pid: int):
+        if my_pid in seen:
+            return any(pid != my_pid for pid in seen)
+        return len(seen) > 1
+
+    def summary(self):
+        if self.proc is None or not self.out.strip():
+            return None
+        seen = self.parse(self.out, os.getpid())
+        samples = sum(1 for line in self.out.splitlines() if line.strip() and not line.lstrip().startswith("#"))
+        return {"foreign_sm_use": self.judge(seen, os.getpid()), "method": "nvidia-smi pmon -s u -d 1, whole run",
+                "samples": samples, "pids_with_sm_use": sorted(seen), "own_pid": os.getpid()}
+
+
 def gpu_index_for_smi(local_rank):
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     if vis:
@@ -212,71 +274,146 @@ def barrier(world: int):
 
 # ------------------------------------------------------------ CPU oracle
 
-def oracle_step_sample(cfg: W.EPConfig, inp: dict, y_bits, tokens: int) -> float:
-    """Seconds for the oracle to run layout + dispatch + combine on the first
-    `tokens` tokens of the workload (the same routing, a bounded sample)."""
+def host_cores() -> int:
+    """The host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def oracle_slice(cfg: W.EPConfig, inp: dict, y_bits, t0: int, t1: int) -> None:
+    """The unchanged oracle's layout, dispatch and combine on tokens
+    [t0, t1) of the workload, as one independent problem."""
     import oracle
-    sub = {k: v[:tokens] for k, v in inp.items()}
+    sub = {k: v[t0:t1] for k, v in inp.items()}
     E, R = cfg.num_experts, cfg.num_ranks
-    t0 = time.perf_counter()
     lay = oracle.get_layout(sub["topk_idx"], E, R)
-    n = int(lay["rank_prefix"][R])
+    n = max(int(lay["rank_prefix"][R]), 1)
     oracle.dispatch(sub["x"], sub["topk_idx"], sub["topk_weights"], E, R, lay["token_slot"],
-                    cfg.fp8, max(n, 1))
-    oracle.combine(y_bits[:max(n, 1)], lay["token_slot"], sub["topk_idx"], sub["topk_weights"], E)
+                    cfg.fp8, n)
+    oracle.combine(y_bits[:n], lay["token_slot"], sub["topk_idx"], sub["topk_weights"], E)
+
+
+def oracle_pass(cfg: W.EPConfig, inp: dict, y_bits, threads: int, pool=None, tokens=None) -> float:
+    """Seconds for one pass of the oracle over the first `tokens` tokens (all
+    by default): the tokens split into `threads` contiguous slices, each
+    slice an independent problem run by the oracle in its own host thread
+    (the oracle's C calls release the interpreter lock)."""
+    T = cfg.num_tokens if tokens is None else tokens
+    bounds = [(T * i // threads, T * (i + 1) // threads) for i in range(threads)]
+    t0 = time.perf_counter()
+    if threads == 1 or pool is None:
+        for a, b in bounds:
+            oracle_slice(cfg, inp, y_bits, a, b)
+    else:
+        list(pool.map(lambda ab: oracle_slice(cfg, inp, y_bits, *ab), bounds))
     return time.perf_counter() - t0
 
 
-def cpu_baseline(cfg, inp, y_bits, budget_s: float = 12.0) -> dict:
-    tokens = min(cfg.num_tokens, 1024)
-    times = []
+def _oracle_rows_needed(cfg: W.EPConfig) -> int:
+    return cfg.num_tokens * min(cfg.num_topk, cfg.num_ranks)
+
+
+def _oracle_y(cfg: W.EPConfig, y_bits):
+    """Expert-output rows for the oracle's combine: the given ones when
+    there are enough, else 4096 seeded rows tiled (the largest workload)."""
+    need = _oracle_rows_needed(cfg)
+    if y_bits is not None and y_bits.shape[0] >= need:
+        return y_bits
+    base = W.expert_output(min(need, 4096), cfg.hidden, seed=1)
+    return base[np.arange(need) % base.shape[0]]
+
+
+def cpu_baseline(cfg, inp, y_bits, budget_s: float = 20.0) -> dict:
+    """The oracle on the whole workload, timed on the host cores: on every
+    core (one token slice per core) and on one thread; medians of repeats
+    within the budget (at least one of each)."""
+    from concurrent.futures import ThreadPoolExecutor
+    cores = host_cores()
+    y_bits = _oracle_y(cfg, y_bits)
+    all_t, one_t = [], []
+    with ThreadPoolExecutor(cores) as pool:
+        t_start = time.perf_counter()
+        while time.perf_counter() - t_start < budget_s / 2 or not all_t:
+            all_t.append(oracle_pass(cfg, inp, y_bits, cores, pool))
     t_start = time.perf_counter()
-    while time.perf_counter() - t_start < budget_s or not times:
-        times.append(oracle_step_sample(cfg, inp, y_bits, tokens))
-    per_call_s = statistics.median(times) * (cfg.num_tokens / tokens)
-    return {"value": per_call_s * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"first {tokens} of {cfg.num_tokens} tokens, {len(times)} reps "
-                      f"(median), scaled by {cfg.num_tokens / tokens:g} to one full step; "
-                      "single-threaded C oracle"}
+    while time.perf_counter() - t_start < budget_s / 2 or not one_t:
+        one_t.append(oracle_pass(cfg, inp, y_bits, 1))
+    med_all, med_one = statistics.median(all_t), statistics.median(one_t)
+    return {"value": round(med_all * 1e6, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"the whole workload ({cfg.num_tokens} tokens) per repeat, median of {len(all_t)}; "
+                       f"the tokens split into {cores} contiguous slices, each slice's layout, dispatch "
+                       "and combine run by the unchanged C oracle in its own host thread"),
+            "single_thread": {"value": round(med_one * 1e6, 1), "unit": UNIT, "cores": 1,
+                              "sample": f"the whole workload per repeat, median of {len(one_t)}"},
+            "cpu_model": cpu_model()}
 
 
 def run_reference(args, rank, world):
-    """`--impl reference`: the oracle as it stands, on the host cores.  Each
-    step runs the oracle on a sample of the workload's tokens, sized so the
-    whole run takes about two minutes, and is scaled to one full step."""
+    """`--impl reference`: the oracle as it stands, on the host cores (one
+    token slice per core).  Each step is one pass over the whole workload,
+    unless the whole --steps + --warmup run would take over ~150 s: then
+    each step takes the workload's first tokens and is scaled to the whole."""
     if rank != 0:
         return 0
     import oracle
+    from concurrent.futures import ThreadPoolExecutor
     cfg = W.CONFIGS[args.workload]
     inp = W.make(cfg)
     # the received rows, for the same config as the GPU arm's line
     n_rows = int(oracle.get_layout(inp["topk_idx"], cfg.num_experts, cfg.num_ranks)["rank_prefix"][cfg.num_ranks])
-    cap_rows = min(cfg.num_tokens, 1024) * min(cfg.num_topk, cfg.num_ranks)
-    y_bits = W.expert_output(max(cap_rows, 1), cfg.hidden, seed=1)
-    probe = min(cfg.num_tokens, 64)
-    t_probe = min(oracle_step_sample(cfg, inp, y_bits, probe) for _ in range(3))
-    per_step_budget = 120.0 / (args.steps + args.warmup)
-    tokens = int(max(8, min(cfg.num_tokens, 1024, probe * per_step_budget / max(t_probe, 1e-9))))
-    for _ in range(args.warmup):
-        oracle_step_sample(cfg, inp, y_bits, tokens)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle_step_sample(cfg, inp, y_bits, tokens)
-    el = time.perf_counter() - t0
-    per_call_us = el / args.steps * (cfg.num_tokens / tokens) * 1e6
-    sample = (f"each step: first {tokens} of {cfg.num_tokens} tokens, scaled by "
-              f"{cfg.num_tokens / tokens:g} to one full step; single-threaded C oracle")
+    y_bits = _oracle_y(cfg, None)
+    cores = host_cores()
+    T = cfg.num_tokens
+    with ThreadPoolExecutor(cores) as pool:
+        probe = min(T, max(cores * 64, T // 8))
+        t_probe = oracle_pass(cfg, inp, y_bits, cores, pool, probe)
+        per_step_budget = 150.0 / (args.steps + args.warmup)
+        tokens = T if t_probe * T / probe <= per_step_budget else \
+            int(max(cores, min(T, probe * per_step_budget / max(t_probe, 1e-9))))
+        for _ in range(args.warmup):
+            oracle_pass(cfg, inp, y_bits, cores, pool, tokens)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle_pass(cfg, inp, y_bits, cores, pool, tokens)
+        el = time.perf_counter() - t0
+    per_call_us = el / args.steps * (T / tokens) * 1e6
+    if tokens == T:
+        sample = (f"each step: the whole workload ({T} tokens), split into {cores} contiguous token "
+                  "slices, each run by the unchanged C oracle in its own host thread")
+    else:
+        sample = (f"each step: the first {tokens} of {T} tokens, split into {cores} contiguous slices "
+                  f"(one host thread each), scaled by {T / tokens:g} to the whole workload")
     line = {"impl": "reference", "metric": METRIC, "value": round(per_call_us, 1), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(per_call_us / 1e3, 3), "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": path_dtype(cfg), "data": "synthetic",
             "config": config_dict(cfg, n_rows),
-            "cpu_baseline": {"value": round(per_call_us, 1), "unit": UNIT, "cores": 1,
-                             "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": round(per_call_us, 1), "unit": UNIT, "cores": cores,
+                             "kind": "oracle", "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": round(per_call_us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def path_dtype(cfg: W.EPConfig) -> str:
+    """The arithmetic the path computes in."""
+    return ("fp8_e4m3 dispatch (fp32 scales) + bf16 combine (fp32 accumulate)" if cfg.fp8
+            else "bf16 dispatch (bit copy) + bf16 combine (fp32 accumulate)")
 
 
 L2_BYTES = 129e6  # GB300 L2
@@ -304,134 +441,233 @@ def config_dict(cfg: W.EPConfig, N: int):
 
 # ------------------------------------------------------------ our path
 
-def run_ours(args, rank, world, local):
-    import combine_ep_get_layout_gb300 as ep
-    from combine_ep_get_layout_gb300 import _native as N_
+class Prepared:
+    """One workload's device tensors and its pre-marshalled C-ABI calls on
+    the current stream: the step (ep_get_layout_and_dispatch, then
+    ep_combine) and the three separate calls (ep_get_layout, ep_dispatch,
+    ep_combine)."""
 
+    def __init__(self, cfg: W.EPConfig, dev, inp=None, y_np=None):
+        import combine_ep_get_layout_gb300 as ep
+        from combine_ep_get_layout_gb300 import _native as N_
+        self.cfg = cfg
+        inp = W.make(cfg) if inp is None else inp
+        E, R, K, T, H = cfg.num_experts, cfg.num_ranks, cfg.num_topk, cfg.num_tokens, cfg.hidden
+        cap = W.recv_capacity(cfg)
+        self.cap = cap
+        self.x = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).to(dev)
+        self.idx = torch.from_numpy(inp["topk_idx"]).to(dev)
+        self.w = torch.from_numpy(inp["topk_weights"]).to(dev)
+        self.lay = ep.ep_get_layout(self.idx, E, R)
+        self.d = ep.ep_dispatch(self.x, self.idx, self.w, self.lay, dtype="fp8" if cfg.fp8 else "bf16",
+                                recv_capacity=cap)
+        self.n_rows = self.lay.num_recv()
+        if y_np is not None:  # the expert output: given rows
+            self.y = torch.from_numpy(y_np.view(np.int16)).view(torch.bfloat16).to(dev)
+        else:  # 4096 seeded bf16 N(0,1) rows tiled over the received rows, built on the device
+            base = torch.from_numpy(W.expert_output(4096, H, seed=1).view(np.int16)).view(torch.bfloat16).to(dev)
+            self.y = base[torch.arange(max(self.n_rows, 1), device=dev) % 4096]
+        self.out = ep.ep_combine(self.y, self.lay, self.idx, self.w)
+        torch.cuda.synchronize()
+        assert self.lay.errors() == 0, self.lay.errors()
+
+        lib = N_.load()
+        self.lib = lib
+        self.stream = torch.cuda.current_stream(dev)
+        sp = C.c_void_p(self.stream.cuda_stream)
+        st = self.lay.c_struct()
+        self._st = st
+        p = lambda t: C.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+        d = self.d
+        self.a_layout = (p(self.idx), T, K, E, R, C.byref(st), p(self.lay.workspace),
+                         self.lay.workspace.numel(), sp)
+        self.a_dispatch = (p(self.x), T, H, p(self.idx), p(self.w), K, E, R, C.byref(st),
+                           N_.EP_DTYPE_FP8_E4M3 if cfg.fp8 else N_.EP_DTYPE_BF16, p(d.recv_x),
+                           p(d.recv_x_scales), p(d.recv_src_idx), p(d.recv_topk_idx),
+                           p(d.recv_topk_weights), cap, sp)
+        self.a_combine = (p(self.y), self.y.shape[0], H, C.byref(st), T, R, p(self.idx), p(self.w), K, E,
+                          p(self.out), sp)
+        val = lambda v: v.value if isinstance(v, C.c_void_p) else v  # noqa: E731
+        self._d_args = N_.ep_dispatch_args_t(*(val(v) for v in self.a_dispatch[:8]), C.pointer(st),
+                                             *(val(v) for v in self.a_dispatch[9:16]), None)
+        self.a_layout_dispatch = (C.byref(self._d_args), p(self.lay.workspace), self.lay.workspace.numel(), sp)
+
+    def _ok(self, *status):
+        if any(status):
+            raise RuntimeError(f"status {status}: {self.lib.ep_last_error().decode()}")
+
+    def step(self):
+        """One step: the layout and the dispatch as one call (the dispatch
+        loading its first rows while the layout runs), then the combine."""
+        self._ok(self.lib.ep_get_layout_and_dispatch(*self.a_layout_dispatch),
+                 self.lib.ep_combine(*self.a_combine))
+
+    def layout(self):
+        self._ok(self.lib.ep_get_layout(*self.a_layout))
+
+    def dispatch(self):
+        self._ok(self.lib.ep_dispatch(*self.a_dispatch))
+
+    def combine(self):
+        self._ok(self.lib.ep_combine(*self.a_combine))
+
+    def launches_per_step(self) -> int:
+        """Kernels one step launches: the one-launch layout (up to 524 288
+        tokens, else the two layout kernels), the dispatch, the combine."""
+        return 3 if 0 < self.cfg.num_tokens <= 2048 * 256 else 4
+
+    def time_steps(self, steps: int) -> float:
+        """ms per step, back to back, CUDA events on the stream."""
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        ev0.record(self.stream)
+        for _ in range(steps):
+            self.step()
+        ev1.record(self.stream)
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1) / steps
+
+    def time_kernels(self, steps: int) -> dict:
+        """Mean ms of each call (layout, dispatch, combine) with an event
+        between calls, so each includes its own launch."""
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        torch.cuda.synchronize()
+        for e in evs:
+            e[0].record(self.stream)
+            self.layout()
+            e[1].record(self.stream)
+            self.dispatch()
+            e[2].record(self.stream)
+            self.combine()
+            e[3].record(self.stream)
+        torch.cuda.synchronize()
+        return {nm: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
+                for j, nm in enumerate(KERNEL_NAMES)}
+
+
+KERNEL_NAMES = ("layout", "dispatch", "combine")
+
+
+def kernel_entries(cfg, n_rows, per_kernel_ms, peak, peak_kind) -> dict:
+    abytes = algorithmic_bytes(cfg, n_rows)
+    out = {}
+    for nm in KERNEL_NAMES:
+        us = per_kernel_ms[nm] * 1e3
+        gbs = abytes[nm] / (us * 1e-6) / 1e9
+        out[nm] = {"us": round(us, 2), "kernel": kernel_symbol(nm, cfg), "algorithmic_bytes": abytes[nm],
+                   "gbs": round(gbs, 1), "frac_of_" + peak_kind + "_peak": round(gbs / peak, 4)}
+    return out
+
+
+def measure_workload(cfg: W.EPConfig, dev, peak: float, peak_kind: str, steps: int = 300,
+                     warmup: int = 10) -> dict:
+    """One workload's step and per-call times (secondary numbers beside the
+    headline), its inputs freed afterwards."""
+    pw = Prepared(cfg, dev)
+    for _ in range(warmup):
+        pw.step()
+    step_ms = pw.time_steps(steps)
+    per = pw.time_kernels(min(steps, 200))
+    assert pw.lay.errors() == 0
+    abytes = algorithmic_bytes(cfg, pw.n_rows)
+    step_gbs = sum(abytes.values()) / (step_ms * 1e-3) / 1e9
+    res = {"recv_rows": pw.n_rows, "step_us": round(step_ms * 1e3, 2),
+           "step_frac_of_" + peak_kind + "_peak": round(step_gbs / peak, 4),
+           "kernels": kernel_entries(cfg, pw.n_rows, per, peak, peak_kind),
+           "steps": steps, "l2": l2_note(cfg, pw.n_rows)}
+    del pw
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     cfg = W.CONFIGS[args.workload]
     inp = W.make(cfg)
-    E, R, K, T, H = cfg.num_experts, cfg.num_ranks, cfg.num_topk, cfg.num_tokens, cfg.hidden
-    cap = W.recv_capacity(cfg)
+    y_np = W.expert_output(W.recv_capacity(cfg), cfg.hidden, seed=1)
+    with GpuProcessSampler(gpu_index_for_smi(local)) as procs:
+        pw = Prepared(cfg, dev, inp=inp, y_np=y_np)
+        n_rows = pw.n_rows
 
-    x = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).to(dev)
-    idx = torch.from_numpy(inp["topk_idx"]).to(dev)
-    w = torch.from_numpy(inp["topk_weights"]).to(dev)
-    lay = ep.ep_get_layout(idx, E, R)
-    d = ep.ep_dispatch(x, idx, w, lay, dtype="fp8" if cfg.fp8 else "bf16", recv_capacity=cap)
-    n_rows = lay.num_recv()
-    y_np = W.expert_output(cap, H, seed=1)
-    y = torch.from_numpy(y_np.view(np.int16)).view(torch.bfloat16).to(dev)
-    out = ep.ep_combine(y, lay, idx, w)
-    torch.cuda.synchronize()
-    assert lay.errors() == 0, lay.errors()
-
-    # Pre-marshalled C-ABI calls on the current stream.
-    lib = N_.load()
-    stream = torch.cuda.current_stream(dev)
-    sp = C.c_void_p(stream.cuda_stream)
-    st = lay.c_struct()
-    p = lambda t: C.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
-    a_layout = (p(idx), T, K, E, R, C.byref(st), p(lay.workspace), lay.workspace.numel(), sp)
-    a_dispatch = (p(x), T, H, p(idx), p(w), K, E, R, C.byref(st),
-                  N_.EP_DTYPE_FP8_E4M3 if cfg.fp8 else N_.EP_DTYPE_BF16, p(d.recv_x),
-                  p(d.recv_x_scales), p(d.recv_src_idx), p(d.recv_topk_idx),
-                  p(d.recv_topk_weights), cap, sp)
-    a_combine = (p(y), cap, H, C.byref(st), T, R, p(idx), p(w), K, E, p(out), sp)
-    f_layout, f_dispatch, f_combine = lib.ep_get_layout, lib.ep_dispatch, lib.ep_combine
-    # the step: layout and dispatch as one call (two launches, the dispatch
-    # loading its first rows while the layout runs), then the combine
-    d_args = N_.ep_dispatch_args_t(*(v.value if isinstance(v, C.c_void_p) else v for v in a_dispatch[:8]),
-                                   C.pointer(st), *(v.value if isinstance(v, C.c_void_p) else v
-                                                    for v in a_dispatch[9:16]), None)
-    a_layout_dispatch = (C.byref(d_args), p(lay.workspace), lay.workspace.numel(), sp)
-    f_layout_dispatch = lib.ep_get_layout_and_dispatch
-
-    def step():
-        s1 = f_layout_dispatch(*a_layout_dispatch)
-        s3 = f_combine(*a_combine)
-        if s1 or s3:
-            raise RuntimeError(f"status {s1} {s3}: {lib.ep_last_error().decode()}")
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-
-    # (1) K steps, bracketed by barrier + synchronize, timed on the stream.
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(gpu_index_for_smi(local)) as clocks:
-        barrier(world)
+        for _ in range(args.warmup):
+            pw.step()
         torch.cuda.synchronize()
-        t_wall = time.perf_counter()
-        ev0.record(stream)
-        for _ in range(args.steps):
-            step()
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall
-        barrier(world)
-    ms_per_step = ev0.elapsed_time(ev1) / args.steps
-    ms_per_step = max_over_ranks(ms_per_step, world)
-    # layout (one launch up to 524 288 tokens, else count and slots),
-    # dispatch, combine
-    launches = (3 if 0 < T <= 2048 * 256 else 4) * args.steps
 
-    # (2) the same steps with an event between kernels: per-kernel durations.
-    k_steps = min(args.steps, 500)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(k_steps)]
-    torch.cuda.synchronize()
-    for e in evs:
-        e[0].record(stream)
-        f_layout(*a_layout)
-        e[1].record(stream)
-        f_dispatch(*a_dispatch)
-        e[2].record(stream)
-        f_combine(*a_combine)
-        e[3].record(stream)
-    torch.cuda.synchronize()
-    names = ["layout", "dispatch", "combine"]
-    per_kernel_ms = {nm: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
-                     for j, nm in enumerate(names)}
-    assert lay.errors() == 0
+        # (1) K steps, bracketed by barrier + synchronize, timed on the stream.
+        stream = pw.stream
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(gpu_index_for_smi(local)) as clocks:
+            barrier(world)
+            torch.cuda.synchronize()
+            t_wall = time.perf_counter()
+            ev0.record(stream)
+            for _ in range(args.steps):
+                pw.step()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            t_wall = time.perf_counter() - t_wall
+            barrier(world)
+        ms_per_step = ev0.elapsed_time(ev1) / args.steps
+        ms_per_step = max_over_ranks(ms_per_step, world)
+        launches = pw.launches_per_step() * args.steps
 
-    peak, peak_kind = hbm_peak()
-    abytes = algorithmic_bytes(cfg, n_rows)
-    kernels = {}
-    for nm in names:
-        us = per_kernel_ms[nm] * 1e3
-        gbs = abytes[nm] / (us * 1e-6) / 1e9
-        kernels[nm] = {"us": round(us, 2), "algorithmic_bytes": abytes[nm], "gbs": round(gbs, 1),
-                       "frac_of_" + peak_kind + "_peak": round(gbs / peak, 4)}
-    dom = max(names, key=lambda nm: per_kernel_ms[nm])
-    dom_gbs = abytes[dom] / (per_kernel_ms[dom] * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": kernel_symbol(dom, cfg), "achieved": round(dom_gbs, 1),
-                "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                "frac": round(dom_gbs / peak, 4), "traffic": ncu_traffic(dom, cfg),
-                "algorithmic_bytes_per_launch": abytes[dom]}
-    step_bytes = sum(abytes.values())
-    step_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
+        # (2) the same steps with an event between calls: per-call durations.
+        per_kernel_ms = pw.time_kernels(min(args.steps, 500))
+        assert pw.lay.errors() == 0
 
-    # (3) end to end through the public binding, host buffers, copies included.
-    e2e = None if args.no_e2e else run_e2e(args, cfg, inp, y_np, cap, dev, world)
+        peak, peak_kind = hbm_peak()
+        abytes = algorithmic_bytes(cfg, n_rows)
+        kernels = kernel_entries(cfg, n_rows, per_kernel_ms, peak, peak_kind)
+        dom = max(KERNEL_NAMES, key=lambda nm: per_kernel_ms[nm])
+        dom_gbs = abytes[dom] / (per_kernel_ms[dom] * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": kernel_symbol(dom, cfg), "achieved": round(dom_gbs, 1),
+                    "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                    "frac": round(dom_gbs / peak, 4), "traffic": ncu_traffic(dom, cfg),
+                    "algorithmic_bytes_per_launch": abytes[dom]}
+        step_bytes = sum(abytes.values())
+        step_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
 
-    # (4) the next rows (cached layout, packed rows, expanded path, bias and
-    # stats) on the same workload: secondary numbers, after the timed region.
-    next_rows = None if (args.no_next_rows or not cfg.fp8) else run_next_rows(cfg, x, idx, w, y, cap, lay, peak)
+        # (3) end to end through the public binding, host buffers, copies included.
+        e2e = None if args.no_e2e else run_e2e(args, cfg, inp, y_np, pw.cap, dev, world)
+
+        # (4) the next rows (cached layout, packed rows, expanded path, bias and
+        # stats) on the same workload: secondary numbers, after the timed region.
+        next_rows = None if (args.no_next_rows or not cfg.fp8) else \
+            run_next_rows(cfg, pw.x, pw.idx, pw.w, pw.y, pw.cap, pw.lay, peak)
+        head = {"recv_rows": n_rows, "step_us": round(ms_per_step * 1e3, 2),
+                "step_frac_of_" + peak_kind + "_peak": round(step_gbs / peak, 4),
+                "kernels": kernels, "steps": args.steps, "l2": l2_note(cfg, n_rows)}
+        del pw
+        torch.cuda.empty_cache()
+
+        # (5) every workload, the same step and calls (secondary numbers).
+        workloads = None
+        if not args.no_workloads:
+            workloads = {}
+            for name, c in W.CONFIGS.items():
+                workloads[name] = head if name == cfg.name else measure_workload(c, dev, peak, peak_kind)
 
     if rank != 0:
         return 0
     line = {
         "metric": METRIC, "value": round(ms_per_step * 1e3, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": path_dtype(cfg),
         "data": "synthetic", "config": config_dict(cfg, n_rows),
         "gbs": round(step_gbs, 1), "frac_of_hbm_peak": round(step_gbs / peak, 4),
-        "kernels": kernels, "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
-        "clocks": clocks.summary(), "wall_s_timed_region": round(t_wall, 4),
+        "kernels": kernels,
+        "step_kernels": [("layout_local_kernel" if 0 < cfg.num_tokens <= 2048 * 256
+                          else "layout_count_kernel+layout_slot_kernel"),
+                         kernel_symbol("dispatch", cfg), kernel_symbol("combine", cfg)],
+        "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
+        "clocks": clocks.summary(), "gpu_processes": procs.summary(), "wall_s_timed_region": round(t_wall, 4),
     }
+    line["foreign_sm_use"] = line["gpu_processes"]["foreign_sm_use"] if line["gpu_processes"] else None
     if next_rows is not None:
         line["next_rows"] = next_rows
+    if workloads is not None:
+        line["workloads"] = workloads
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, inp, y_np)
     print(json.dumps(line), flush=True)
@@ -600,11 +836,36 @@ def run_e2e(args, cfg, inp, y_np, cap, dev, world):
     us = max_over_ranks(e0.elapsed_time(e1) / steps * 1e3, world)
     h2d = sum(t.numel() * t.element_size() for t in h_in)
     d2h = h_out[0].numel() * h_out[0].element_size()
+
+    # The bound: the same copies alone, the same streams and buffers, no path.
+    def copies(i):
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            for d, h in zip(d_in[b], h_in):
+                d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            h_out[b].copy_(d_out[b], non_blocking=True)
+    for i in range(3):
+        copies(i)
+    torch.cuda.synchronize()
+    c0, c1, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    c0.record(s_in)
+    s_out.wait_event(c0)
+    for i in range(steps):
+        copies(i)
+    c1.record(s_in)
+    c2.record(s_out)
+    torch.cuda.synchronize()
+    copy_us = max(c0.elapsed_time(c1), c0.elapsed_time(c2)) / steps * 1e3
+    copy_us = max_over_ranks(copy_us, world)
     return {"value": round(us, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
+            "copy_only_us": round(copy_us, 2), "frac_of_copy_bound": round(copy_us / us, 4),
+            "h2d_gbs": round(h2d / (copy_us * 1e-6) / 1e9, 1),
             "note": "inputs x, topk_idx, topk_weights and the expert output y copied in, "
                     "the combined rows copied out, every step; steps pipelined over three "
-                    "streams (upload, path, read-back)"}
+                    "streams (upload, path, read-back); copy_only_us: the same copies on the same "
+                    "streams with no path between them (the host link's bound)"}
 
 
 def main(argv=None):
@@ -618,6 +879,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-next-rows", action="store_true",
                     help="skip the secondary timings of the next rows (cached layout, packed, expanded, bias)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the secondary timings of the other workloads")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
     args.steps = max(1, args.steps)

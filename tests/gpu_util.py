@@ -2,10 +2,13 @@
 Python binding (which calls the C ABI) and bring results back as numpy."""
 from __future__ import annotations
 
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
 import combine_ep_get_layout_gb300 as ep
+import oracle
 
 
 def dev():
@@ -33,6 +36,14 @@ def layout_np(lay: ep.Layout) -> dict:
         "token_slot": bits(lay.token_slot),
         "error": int(lay.errors()),
     }
+
+
+def dispatch_np(d) -> dict:
+    """A dispatch's outputs as numpy bit patterns."""
+    return {"recv_x": bits(d.recv_x),
+            "recv_x_scales": None if d.recv_x_scales is None else bits(d.recv_x_scales),
+            "recv_src_idx": bits(d.recv_src_idx), "recv_topk_idx": bits(d.recv_topk_idx),
+            "recv_topk_weights": bits(d.recv_topk_weights)}
 
 
 def run_gpu_path(x_bits, topk_idx, topk_weights, E, R, fp8, cap, y_bits=None,
@@ -125,3 +136,42 @@ def subset_problem(token_ids: np.ndarray, token_slot: np.ndarray):
     pos = np.searchsorted(glob, sub[sub >= 0])
     local[sub >= 0] = pos
     return local.astype(np.int32), glob
+
+
+def check_whole_path_in_chunks(g: dict, inp: dict, token_slot: np.ndarray, E: int, R: int, fp8: bool,
+                               y_rows=None, combine: bool = True, chunk: int = 8192, workers: int = 8):
+    """Every received row and every combined token of a large workload
+    against the oracle, bit for bit, one chunk of consecutive tokens at a
+    time (so the oracle's buffers stay bounded; chunks run in threads, the
+    oracle's C calls release the GIL).
+
+    g: the GPU's outputs as numpy (recv_x, recv_x_scales, recv_src_idx,
+    recv_topk_idx, recv_topk_weights, and combined when `combine`);
+    token_slot: the oracle's layout; y_rows(glob) -> the expert-output rows
+    at those received rows (None: the bf16 round trip combines the
+    dispatched rows).  Returns the number of rows checked (every row once)."""
+    idx, w, x = inp["topk_idx"], inp["topk_weights"], inp["x"]
+    T = idx.shape[0]
+
+    def one(t0):
+        toks = np.arange(t0, min(t0 + chunk, T))
+        local, glob = subset_problem(toks, token_slot)
+        n = len(glob)
+        d_o = oracle.dispatch(x[toks], idx[toks], w[toks], E, R, local, fp8, max(n, 1))
+        assert d_o["error"] == 0
+        d_o["recv_src_idx"] = toks[d_o["recv_src_idx"][:n]]
+        sub = {k: g[k][glob] for k in ("recv_x", "recv_src_idx", "recv_topk_idx", "recv_topk_weights")}
+        sub["recv_x_scales"] = g["recv_x_scales"][glob] if fp8 else None
+        assert_dispatch_equal(sub, d_o, n, fp8)
+        if combine:
+            y = y_rows(glob) if y_rows is not None else d_o["recv_x"][:n]
+            c_o, _ = oracle.combine(y, local, idx[toks], w[toks], E)
+            got = g["combined"][toks]
+            if not np.array_equal(got, c_o):
+                assert_combine_exact(got, c_o)  # reports the first elements that differ
+        return glob
+
+    with ThreadPoolExecutor(workers) as ex:
+        globs = list(ex.map(one, range(0, T, chunk)))
+    rows = np.concatenate(globs) if globs else np.zeros(0, np.int64)
+    return rows

@@ -114,7 +114,61 @@ def test_reference_arm_line_on_the_tiny_workload(capsys):
     assert (line["metric"], line["unit"], line["higher_is_better"]) == (bench.METRIC, bench.UNIT, False)
     assert line["config"] == bench.config_dict(cfg, 229)  # the tiny workload: 229 received rows
     assert line["value"] > 0 and line["steps"] == 2 and line["warmup"] == 3
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == bench.host_cores()
+    assert "whole workload" in line["cpu_baseline"]["sample"]  # the tiny workload fits the time budget
+    assert line["dtype"] == bench.path_dtype(cfg) and "bf16" in line["dtype"]
     assert line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": bench.UNIT,
                            "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_oracle_pass_covers_every_token_once(monkeypatch):
+    """The threaded oracle pass splits the tokens into contiguous slices that
+    cover every token exactly once, whatever the thread count."""
+    from concurrent.futures import ThreadPoolExecutor
+    seen = []
+    monkeypatch.setattr(bench, "oracle_slice", lambda cfg, inp, y, a, b: seen.append((a, b)))
+    cfg = W.CONFIGS["tiny_128x256_top2_16e"]
+    for threads in (1, 3, 8, 16):
+        seen.clear()
+        with ThreadPoolExecutor(threads) as pool:
+            bench.oracle_pass(cfg, {}, None, threads, pool)
+        cover = sorted(seen)
+        assert cover[0][0] == 0 and cover[-1][1] == 128
+        assert all(a[1] == b[0] for a, b in zip(cover, cover[1:]))
+        seen.clear()
+        bench.oracle_pass(cfg, {}, None, threads, None, tokens=100)
+        assert sorted(seen)[-1][1] == 100 and sum(b - a for a, b in seen) == 100
+
+
+def test_cpu_baseline_measures_the_whole_workload():
+    """Both figures time the oracle on every token of the workload (no
+    scaling), on all host cores and on one thread."""
+    cfg = W.CONFIGS["tiny_128x256_top2_16e"]
+    inp = W.make(cfg)
+    y = W.expert_output(W.recv_capacity(cfg), cfg.hidden)
+    cb = bench.cpu_baseline(cfg, inp, y, budget_s=0.5)
+    assert cb["kind"] == "oracle" and cb["cores"] == bench.host_cores() and cb["value"] > 0
+    assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
+    assert "whole workload" in cb["sample"] and "scaled" not in cb["sample"]
+
+
+PMON = """# gpu         pid   type     sm    mem    enc    dec    jpg    ofa    command
+# Idx           #    C/G      %      %      %      %      %      %    name
+    0      41000     C     87     60      -      -      -      -    python
+    0          -     -      -      -      -      -      -      -    -
+    0      41000     C     90     61      -      -      -      -    python
+    0      52000     C      3      1      -      -      -      -    other
+    0      53000     C      -      -      -      -      -      -    idle
+"""
+
+
+def test_gpu_process_sampler_flags_a_foreign_process():
+    seen = bench.GpuProcessSampler.parse(PMON, 41000)
+    assert seen == {41000: 90, 52000: 3}
+    assert bench.GpuProcessSampler.judge(seen, 41000) is True
+    alone = bench.GpuProcessSampler.parse(PMON.split("    0      52000")[0], 41000)
+    assert bench.GpuProcessSampler.judge(alone, 41000) is False
+    # ids of another namespace: this process is one of them, so two are foreign use
+    assert bench.GpuProcessSampler.judge({7: 50}, 41000) is False
+    assert bench.GpuProcessSampler.judge({7: 50, 8: 2}, 41000) is True

@@ -162,8 +162,9 @@ def test_more_tokens_than_the_one_launch_layout_takes():
 
 
 def test_large_workload():
-    """The 65536-token workload: the whole layout and a sample of the rows
-    against the oracle."""
+    """The 65536-token workload through the one call: the whole layout and
+    every received row and its metadata against the oracle (chunks of 8192
+    tokens)."""
     cfg = W.CONFIGS["fp8_65536x7168_top8_256e"]
     inp = W.make(cfg)
     E, R = cfg.num_experts, cfg.num_ranks
@@ -172,13 +173,11 @@ def test_large_workload():
     N = int(lo["rank_prefix"][R])
     lay, d = _run(x, idx, w, E, R, "fp8", N)
     U.assert_layout_equal(U.layout_np(lay), lo)
-    toks = np.unique(np.random.default_rng(1).choice(cfg.num_tokens, 600, replace=False))
-    local, glob = U.subset_problem(toks, lo["token_slot"])
-    o = oracle.dispatch(x[toks], idx[toks], w[toks], E, R, local, True, len(glob))
-    n = len(glob)
-    assert np.array_equal(U.bits(d.recv_x)[glob], o["recv_x"][:n])
-    assert np.array_equal(U.bits(d.recv_x_scales)[glob].view(np.uint32), o["recv_x_scales"][:n].view(np.uint32))
-    assert np.array_equal(U.bits(d.recv_src_idx)[glob], toks[o["recv_src_idx"][:n]])
+    g = {"recv_x": U.bits(d.recv_x[:N]), "recv_x_scales": U.bits(d.recv_x_scales[:N]),
+         "recv_src_idx": U.bits(d.recv_src_idx[:N]), "recv_topk_idx": U.bits(d.recv_topk_idx[:N]),
+         "recv_topk_weights": U.bits(d.recv_topk_weights[:N])}
+    rows = U.check_whole_path_in_chunks(g, inp, lo["token_slot"], E, R, True, combine=False)
+    assert np.array_equal(np.sort(rows), np.arange(N))
 
 
 def test_repeated_and_mixed_with_layout_kernel():
@@ -227,3 +226,37 @@ def test_rows_written_just_before_the_call():
         assert np.array_equal(U.bits(d.recv_x_scales)[:N].view(np.uint32),
                               want[i % 2]["recv_x_scales"][:N].view(np.uint32)), i
     assert lay.errors() == 0
+
+
+def test_rows_made_by_a_kernel_just_before_each_call():
+    """x is produced by an elementwise kernel (a sign flip, torch.neg) on the
+    same stream immediately before each call, with no synchronisation inside
+    the loop and one output buffer per call: the rows each dispatch loads
+    before its wait for the layout must be that kernel's output.  The layout
+    kernel starts only once the producer has finished, and the dispatch only
+    once the layout has started, so every call must see its own x (checked
+    against the oracle after one final synchronisation)."""
+    T, H, K, E, R = 8192, 2048, 8, 64, 8
+    idx, w, rng = _routing(T, K, E, 15, p_mask=0.0)
+    srcs = [W.normal_bf16(rng, (T, H)) for _ in range(3)]
+    lo = oracle.get_layout(idx, E, R)
+    N = int(lo["rank_prefix"][R])
+    calls = 12
+    xs = [srcs[i % 3] ^ np.uint16(0x8000) for i in range(3)]  # what the sign flip makes
+    want = [oracle.dispatch(x, idx, w, E, R, lo["token_slot"], True, N) for x in xs]
+    d_srcs = [U.to_dev_bf16(x) for x in srcs]
+    d_x = torch.empty_like(d_srcs[0])
+    d_idx, d_w = torch.from_numpy(idx).to(U.dev()), torch.from_numpy(w).to(U.dev())
+    lay, d0 = ep.ep_get_layout_and_dispatch(d_x.zero_(), d_idx, d_w, E, R, dtype="fp8", recv_capacity=N)
+    outs = [ep.ep_get_layout_and_dispatch(d_x, d_idx, d_w, E, R, layout=lay, dtype="fp8",
+                                          recv_capacity=N)[1] for _ in range(calls)]
+    torch.cuda.synchronize()
+    for i in range(calls):
+        torch.neg(d_srcs[i % 3], out=d_x)
+        ep.ep_get_layout_and_dispatch(d_x, d_idx, d_w, E, R, layout=lay, dtype="fp8", recv_capacity=N,
+                                      out=outs[i])
+    torch.cuda.synchronize()
+    assert lay.errors() == 0
+    U.assert_layout_equal(U.layout_np(lay), lo)
+    for i in range(calls):
+        U.assert_dispatch_equal(U.dispatch_np(outs[i]), want[i % 3], N, True)
