@@ -240,11 +240,15 @@ ep_status_t ep_get_layout_and_dispatch(const ep_dispatch_args_t *args, void *wor
     // One layout launch; the dispatch finishes the slots (adds each block's
     // base, writes them back) and counts the experts as it moves the rows.
     const int32_t *local_base = nullptr;
+    int table_blocks = 0;
     EP_CHECK(launch_layout_local(args->topk_idx, a.num_tokens, a.num_topk, a.num_experts, a.num_ranks, *layout,
-                                 workspace, s, &local_base));
+                                 workspace, s, &local_base, &table_blocks));
     a.local_base = local_base;
+    a.local_table_blocks = table_blocks;
     a.token_slot_out = layout->token_slot;
     a.num_tokens_per_expert = layout->num_tokens_per_expert;
+    a.rank_prefix = layout->rank_prefix;
+    a.num_tokens_per_rank = layout->num_tokens_per_rank;
   } else {
     EP_CHECK(launch_layout(args->topk_idx, a.num_tokens, a.num_topk, a.num_experts, a.num_ranks, *layout, workspace,
                            s));

@@ -315,13 +315,15 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
     fence_barrier_init();
   }
   __syncthreads();
-  if (kWarmTokens > 0 && warp == 0) {
+  if (kWarmTokens > 0 && warp == 1) {
     // Before the wait for the kernel ahead, nothing is read for its value:
     // the first tokens' metadata and the first chunks of their rows are only
     // brought into L2.  The first tickets go to tokens 0, 1, ... in some
     // order, so block b warms tokens b, b + gridDim.x, ...  The slots read
     // here may be stale; they serve as addresses only, checked against the
-    // capacity.
+    // capacity.  A reducer warp does it, so that the loader, when the kernel
+    // ahead has already finished, draws its first token without waiting for
+    // these slot reads.
     for (int k = 0; k < kWarmTokens; ++k) {
       const int t = (int)blockIdx.x + k * (int)gridDim.x;
       if (t >= p.T) break;

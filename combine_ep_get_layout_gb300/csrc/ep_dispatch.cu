@@ -65,7 +65,20 @@ struct DispatchParams {
   const int32_t *local_base;
   int32_t *token_slot_out;
   int32_t *num_tokens_per_expert;
+  // table mode (table_blocks = G > 0): local_base holds each 256-token
+  // block's per-rank totals; the storer scans them into shared memory at
+  // table_offset (bases [G*R], rank totals [R], rank offsets [R+1]) and
+  // block 0 writes rank_prefix and num_tokens_per_rank
+  int table_blocks;
+  uint32_t table_offset;
+  int32_t *rank_prefix;
+  int32_t *num_tokens_per_rank;
 };
+
+// Shared-memory bytes of the table mode's scan (see DispatchParams).
+inline uint32_t base_table_bytes(int table_blocks, int R) {
+  return table_blocks > 0 ? ((uint32_t)(table_blocks * R + 2 * R + 1) * 4u + 15u) / 16u * 16u : 0u;
+}
 
 // Token ids travel from the loading thread to the other roles of a block
 // through a ring of kTokRing shared ints: the block's idx-th token (or -1,
@@ -478,6 +491,42 @@ __device__ __forceinline__ void dispatch_ws_body(const DispatchParams &p) {
     if (p.early > 0) griddep_wait();
     const bool scale_bulk = p.scale_stride == (uint32_t)p.groups * 4u &&
                             (reinterpret_cast<uintptr_t>(p.recv_x_scales) & 15u) == 0;
+    // Table mode: the layout left each 256-token block's per-rank totals;
+    // each rank's exclusive scan over the blocks, plus the rank's offset
+    // (the exclusive scan of the rank totals), is each block's base.
+    int32_t *s_base = reinterpret_cast<int32_t *>(smem + p.table_offset);  // [G * R]
+    int32_t *s_rtot = s_base + p.table_blocks * p.R;                        // [R]
+    int32_t *s_roff = s_rtot + p.R;                                         // [R + 1]
+    if (p.table_blocks > 0) {
+      const int G = p.table_blocks, R = p.R;
+      for (int q = lane; q < G * R; q += kWarpSize) s_base[q] = __ldcg(p.local_base + q);
+      __syncwarp();
+      for (int r = lane; r < R; r += kWarpSize) {
+        int run = 0;
+        for (int bb = 0; bb < G; ++bb) {
+          const int v = s_base[bb * R + r];
+          s_base[bb * R + r] = run;
+          run += v;
+        }
+        s_rtot[r] = run;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        int acc = 0;
+        for (int r = 0; r < R; ++r) {
+          s_roff[r] = acc;
+          acc += s_rtot[r];
+        }
+        s_roff[R] = acc;
+      }
+      __syncwarp();
+      if (blockIdx.x == 0) {
+        for (int r = lane; r <= R; r += kWarpSize) {
+          p.rank_prefix[r] = s_roff[r];
+          if (r < R) p.num_tokens_per_rank[r] = s_rtot[r];
+        }
+      }
+    }
     for (int i = 0; !*s_abort; ++i) {
       const int t = wait_token(&s_tok[i % kTokRing]);
       if (t == kTokTimedOut) {
@@ -502,11 +551,17 @@ __device__ __forceinline__ void dispatch_ws_body(const DispatchParams &p) {
       const int64_t e = lane < p.K ? __ldg(p.topk_idx + (size_t)t * p.K + lane) : -1;
       const float w = (lane < p.K && p.recv_topk_weights != nullptr)
                           ? __ldg(p.topk_weights + (size_t)t * p.K + lane) : 0.0f;
-      // local layout: the block's bases, loaded alongside the slots
+      // local layout: the block's bases, loaded alongside the slots (or
+      // taken from the scanned table)
       const size_t blk = (size_t)(t / kLocalTokensPerBlock) * p.R;
-      const int base_lo = (p.local_base != nullptr && lane < p.D) ? __ldg(p.local_base + blk + lane) : 0;
-      const int base_hi = (p.local_base != nullptr && lane + kWarpSize < p.D)
-                              ? __ldg(p.local_base + blk + lane + kWarpSize) : 0;
+      int base_lo = 0, base_hi = 0;
+      if (p.table_blocks > 0) {
+        if (lane < p.D) base_lo = s_base[blk + lane] + s_roff[lane];
+        if (lane + kWarpSize < p.D) base_hi = s_base[blk + lane + kWarpSize] + s_roff[lane + kWarpSize];
+      } else if (p.local_base != nullptr) {
+        if (lane < p.D) base_lo = __ldg(p.local_base + blk + lane);
+        if (lane + kWarpSize < p.D) base_hi = __ldg(p.local_base + blk + lane + kWarpSize);
+      }
       if (p.local_base != nullptr) {
         // finish the layout of token t: absolute slots, written back; its
         // experts counted; ids outside [-1, E) flagged
@@ -684,7 +739,8 @@ ep_status_t launch_ws(DispatchParams &p, const DeviceInfo &di, cudaStream_t stre
   }
   p.stages = kWsStages;
   while (p.stages > 2 && ws_smem_bytes(p) > kWsSmemBudget) --p.stages;
-  const size_t smem = ws_smem_bytes(p);
+  p.table_offset = (uint32_t)ws_smem_bytes(p);
+  const size_t smem = ws_smem_bytes(p) + base_table_bytes(p.table_blocks, p.R);
   if (smem > di.max_smem_per_block_optin)
     return fail(EP_ERR_UNSUPPORTED, "ep_dispatch: hidden %d needs %zu bytes of shared memory", p.H, smem);
   int per_sm = 0;
@@ -713,7 +769,8 @@ ep_status_t launch_ws_bf16(DispatchParams &p, const DeviceInfo &di, cudaStream_t
   auto smem_of = [&](int stages) { return kHeaderBytes + (size_t)stages * p.stage_stride; };
   p.stages = kWsBf16Stages;
   while (p.stages > 2 && smem_of(p.stages) > kWsBf16SmemBudget) --p.stages;
-  const size_t smem = smem_of(p.stages);
+  p.table_offset = (uint32_t)smem_of(p.stages);
+  const size_t smem = smem_of(p.stages) + base_table_bytes(p.table_blocks, p.R);
   if (smem > di.max_smem_per_block_optin)
     return fail(EP_ERR_UNSUPPORTED, "ep_dispatch: hidden %d needs %zu bytes of shared memory", p.H, smem);
   int per_sm = 0;
@@ -908,6 +965,9 @@ ep_status_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream) {
   p.local_base = a.local_base;
   p.token_slot_out = a.token_slot_out;
   p.num_tokens_per_expert = a.num_tokens_per_expert;
+  p.table_blocks = a.local_base != nullptr ? a.local_table_blocks : 0;
+  p.rank_prefix = a.rank_prefix;
+  p.num_tokens_per_rank = a.num_tokens_per_rank;
   ep_status_t st = EP_OK;
   if (a.num_tokens > 0) {
     // packed rows are only built by the warp-specialised kernel

@@ -49,18 +49,23 @@ ep_status_t launch_layout(const int64_t *topk_idx, int num_tokens, int num_topk,
                           int num_ranks, const ep_layout_t &layout, void *workspace,
                           cudaStream_t stream);
 
-// The first half of a layout whose slots the fp8 dispatch finishes
+// The first half of a layout whose slots the dispatch finishes
 // (ep_get_layout_and_dispatch): one launch writes is_token_in_rank, each
 // (token, rank)'s slot relative to its 256-token block into token_slot, and
-// in the workspace each block's first slot in each rank (*local_base, [G*R],
-// G = ceil(T / 256)); rank_prefix and num_tokens_per_rank are final.  The
-// dispatch adds the block's base to each slot, writes it back and counts
-// num_tokens_per_expert and bad ids.  Applies to 0 < T <= local_layout_max_tokens().
+// in the workspace (*local_base, [G*R], G = ceil(T / 256)) either each
+// block's per-rank totals (*table_blocks = G > 0: G*R <= kBaseTableMax; the
+// dispatch scans them itself and writes rank_prefix and
+// num_tokens_per_rank), or, for larger layouts (*table_blocks = 0), each
+// block's first slot in each rank, with rank_prefix and num_tokens_per_rank
+// final.  The dispatch adds the block's base to each slot, writes it back
+// and counts num_tokens_per_expert and bad ids.  Applies to
+// 0 < T <= local_layout_max_tokens().
 int local_layout_max_tokens();
 constexpr int kLocalTokensPerBlock = 256;
+constexpr int kBaseTableMax = 1024;  // block totals the dispatch scans itself (G * R)
 ep_status_t launch_layout_local(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
                                 int num_ranks, const ep_layout_t &layout, void *workspace, cudaStream_t stream,
-                                const int32_t **local_base);
+                                const int32_t **local_base, int *table_blocks);
 
 // ---- expanded layout (ep_layout_expanded.cu)
 size_t expanded_layout_workspace_bytes(int num_tokens, int num_experts);
@@ -102,12 +107,18 @@ struct DispatchArgs {
   // fp8 rows: tokens per block loaded and cast before the wait for the
   // previous kernel on the stream; only when that kernel writes none of x
   int early_rows = 0;
-  // after launch_layout_local (fp8 rows only): token_slot holds slots
-  // relative to each 256-token block; the dispatch adds local_base[b * R + r],
-  // writes the slot back to token_slot_out and counts num_tokens_per_expert
+  // after launch_layout_local: token_slot holds slots relative to each
+  // 256-token block; the dispatch adds the block's base, writes the slot back
+  // to token_slot_out and counts num_tokens_per_expert.  The base is
+  // local_base[b * R + r], or with local_table_blocks = G > 0 it is derived
+  // from the per-block totals at local_base by the dispatch itself, which
+  // then also writes rank_prefix and num_tokens_per_rank.
   const int32_t *local_base = nullptr;
+  int local_table_blocks = 0;
   int32_t *token_slot_out = nullptr;
   int32_t *num_tokens_per_expert = nullptr;
+  int32_t *rank_prefix = nullptr;
+  int32_t *num_tokens_per_rank = nullptr;
 };
 // early_rows of ep_get_layout_and_dispatch (the input stages and the output
 // buffers of the warp-specialised kernel hold up to 5 tokens)

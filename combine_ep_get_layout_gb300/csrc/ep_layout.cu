@@ -18,9 +18,10 @@
 //            over warps give each (token, rank) its slot in ascending token
 //            order (a stable scatter).
 //
-// layout_local_kernel is the one-launch layout of ep_get_layout_and_dispatch
-// (fp8 rows): slots relative to each 256-token block, and the blocks' bases
-// from the last block to finish; the dispatch adds the bases.
+// layout_local_kernel is the one-launch layout of ep_get_layout_and_dispatch:
+// slots relative to each 256-token block and the blocks' per-rank totals,
+// which the dispatch scans itself (up to kBaseTableMax totals) or the last
+// block to finish turns into bases; the dispatch adds the bases.
 #include <algorithm>
 
 #include "ep_device.cuh"
@@ -62,6 +63,19 @@ __device__ __forceinline__ uint64_t rank_mask(const int64_t (&ids)[KMAX], int K,
   return mask;
 }
 
+// Brings the ids of tokens [t0, t0 + n) into L2 without reading them (safe
+// before the wait for the kernel ahead, which may be the one writing them:
+// L2 is where its writes land): one prefetch per 128-byte line, the first
+// kPrefetchIdBytes of the range at most.
+constexpr size_t kPrefetchIdBytes = 64 * 1024;
+__device__ __forceinline__ void prefetch_ids(const LayoutParams &p, int t0, int n) {
+  if (n <= 0) return;
+  const char *base = reinterpret_cast<const char *>(p.topk_idx + (size_t)t0 * p.num_topk);
+  const size_t bytes = min((size_t)n * p.num_topk * sizeof(int64_t), kPrefetchIdBytes);
+  for (size_t off = (size_t)threadIdx.x * 128; off < bytes; off += (size_t)blockDim.x * 128) prefetch_l2(base + off);
+  if (threadIdx.x == 0) prefetch_l2(base + bytes - 1);  // the last line, when base is not line-aligned
+}
+
 // The K ids of token t, all requested before the first is used; -1 past K
 // and for t >= end.
 template <int KMAX>
@@ -79,6 +93,9 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_count_kernel(LayoutPara
   const int b = blockIdx.x;
   const int R = p.num_ranks, E = p.num_experts;
   for (int r = tid; r < R; r += kLayoutThreads) blk_cnt[r] = 0;
+  const int begin = min(b * p.tokens_per_block, p.num_tokens);
+  const int end = min(begin + p.tokens_per_block, p.num_tokens);
+  prefetch_ids(p, begin, end - begin);
   __syncthreads();
   griddep_wait();
   griddep_launch_dependents();
@@ -87,8 +104,6 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_count_kernel(LayoutPara
     if (tid == 0) *p.out.error_word = 0u;
     if (tid < EP_WORK_COUNTER_WORDS && p.out.work_counters != nullptr) p.out.work_counters[tid] = 0u;
   }
-  const int begin = min(b * p.tokens_per_block, p.num_tokens);
-  const int end = min(begin + p.tokens_per_block, p.num_tokens);
   bool bad = false;
   for (int c0 = begin; c0 < end; c0 += kLayoutThreads) {
     int64_t ids[KMAX];
@@ -246,18 +261,22 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_slot_kernel(LayoutParam
 }
 
 // ------------------------------------------------------------------------
-// The first half of a layout that the fp8 dispatch finishes (see
+// The first half of a layout that the dispatch finishes (see
 // launch_layout_local).  One block per 256 tokens (one per thread): the rank
 // masks, each (token, rank)'s slot relative to the block (ballot prefix plus
 // a shared scan over warps, ascending token order), is_token_in_rank, and
-// the block's totals.  The last block to finish (a ticket on `done`, after a
-// fence) turns the totals into each block's first slot in each rank, in
-// place, and writes rank_prefix and num_tokens_per_rank; it leaves `done` at
-// zero for the next call.
-template <int KMAX>
+// the block's totals.  The ids are prefetched into L2 before the wait for
+// the kernel ahead.
+//   SCAN = false: that is all; the dispatch, once this kernel has
+//     completed, scans the totals itself (a small table: G * R entries).
+//   SCAN = true: the totals go out first, then a ticket on `done` (after a
+//     fence); the last block to take one turns the totals into each block's
+//     first slot in each rank, in place, and writes rank_prefix and
+//     num_tokens_per_rank, while the other blocks write their slots.  It
+//     leaves `done` at zero for the next call.
+template <int KMAX, bool SCAN>
 __global__ void __launch_bounds__(kLayoutThreads) layout_local_kernel(LayoutParams p, uint32_t *done) {
   __shared__ int warp_off[kLayoutWarps * EP_MAX_RANKS];
-  __shared__ int blk_tot[EP_MAX_RANKS];
   __shared__ int seg_sum[kLayoutThreads];
   __shared__ int tot[EP_MAX_RANKS];
   __shared__ int base[EP_MAX_RANKS + 1];
@@ -268,6 +287,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_local_kernel(LayoutPara
   const int G = gridDim.x;
   const int b = blockIdx.x;
   const int R = p.num_ranks, E = p.num_experts;
+  prefetch_ids(p, b * kLayoutThreads, min(kLayoutThreads, p.num_tokens - b * kLayoutThreads));
   griddep_wait();
   griddep_launch_dependents();
   if (b == 0) {  // the dispatch adds into them, after this kernel
@@ -292,9 +312,15 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_local_kernel(LayoutPara
       warp_off[w * R + r] = acc;
       acc += c;
     }
-    blk_tot[r] = acc;
+    p.partial[(size_t)b * R + r] = acc;
   }
+  // With SCAN the totals are visible before the ticket; the slots are
+  // written after it (the dispatch reads them once this kernel has
+  // completed), so the last block's pass overlaps the other blocks' slot
+  // writes.
+  if constexpr (SCAN) __threadfence();
   __syncthreads();
+  if (SCAN && tid == 0) s_last = atomicAdd(done, 1u) == (uint32_t)G - 1u;
   const uint32_t lanes_below = (1u << lane) - 1u;
   const bool vec4 = (R % 4) == 0;
   int32_t *slot_row = p.out.token_slot + (size_t)t * R;
@@ -325,13 +351,10 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_local_kernel(LayoutPara
       }
     }
   }
-  for (int r = tid; r < R; r += kLayoutThreads) p.partial[(size_t)b * R + r] = blk_tot[r];
+  if constexpr (!SCAN) return;
 
   // The last block: bases.  Thread (q, r) owns a contiguous run of blocks
   // for rank r; run sums, then their exclusive scan, then the running bases.
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(done, 1u) == (uint32_t)G - 1u;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
@@ -426,7 +449,7 @@ int local_layout_max_tokens() { return kMaxLayoutBlocks * kLocalTokensPerBlock; 
 
 ep_status_t launch_layout_local(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
                                 int num_ranks, const ep_layout_t &layout, void *workspace, cudaStream_t stream,
-                                const int32_t **local_base) {
+                                const int32_t **local_base, int *table_blocks) {
   static_assert(kLocalTokensPerBlock == kLayoutThreads, "one token per thread");
   LayoutParams p;
   const int grid = (num_tokens + kLocalTokensPerBlock - 1) / kLocalTokensPerBlock;
@@ -440,11 +463,20 @@ ep_status_t launch_layout_local(const int64_t *topk_idx, int num_tokens, int num
   p.out = layout;
   p.partial = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(workspace) + kPartialOffset);
   uint32_t *done = static_cast<uint32_t *>(workspace);  // zero between calls
-  cudaError_t e = num_topk > 8
-                      ? launch_kernel(layout_local_kernel<EP_MAX_TOPK>, grid, kLayoutThreads, 0, stream, false, p, done)
-                      : launch_kernel(layout_local_kernel<8>, grid, kLayoutThreads, 0, stream, false, p, done);
+  // A small table of block totals is scanned by the dispatch itself: no
+  // fence, ticket or last-block pass on the path the dispatch waits for.
+  const bool table = (size_t)grid * (size_t)num_ranks <= (size_t)kBaseTableMax;
+  const bool wide = num_topk > 8;
+  cudaError_t e;
+  if (table)
+    e = wide ? launch_kernel(layout_local_kernel<EP_MAX_TOPK, false>, grid, kLayoutThreads, 0, stream, false, p, done)
+             : launch_kernel(layout_local_kernel<8, false>, grid, kLayoutThreads, 0, stream, false, p, done);
+  else
+    e = wide ? launch_kernel(layout_local_kernel<EP_MAX_TOPK, true>, grid, kLayoutThreads, 0, stream, false, p, done)
+             : launch_kernel(layout_local_kernel<8, true>, grid, kLayoutThreads, 0, stream, false, p, done);
   if (e != cudaSuccess) return cuda_fail(e, "launch layout_local_kernel");
   *local_base = p.partial;
+  *table_blocks = table ? grid : 0;
   return EP_OK;
 }
 

@@ -109,6 +109,13 @@ CASES = [
     ("fp8_about_3_tokens_per_block", 1900, 1024, 8, 64, 8, "fp8", {}),
     ("fp8_stripes_few_tokens", 50, 512, 4, 16, 4, "fp8", dict(work_counters=False)),
     ("fp8_19457_tokens", 19457, 256, 8, 64, 8, "fp8", {}),
+    # the layout's block totals scanned by the dispatch (at most 1024 of
+    # them: blocks x ranks) or by the layout's last block, on either side
+    ("fp8_table_1024_totals", 128 * 256, 256, 8, 64, 8, "fp8", {}),
+    ("fp8_scan_1032_totals", 128 * 256 + 1, 256, 8, 64, 8, "fp8", {}),
+    ("bf16_table_R64_1024_totals", 16 * 256, 128, 8, 128, 64, "bf16", {}),
+    ("bf16_scan_R64_1088_totals", 16 * 256 + 1, 128, 8, 128, 64, "bf16", {}),
+    ("bf16_table_R3_ragged", 300 * 256 + 17, 64, 3, 12, 3, "bf16", {}),
 ]
 
 
