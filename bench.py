@@ -529,7 +529,9 @@ class Prepared:
 
     def time_kernels(self, steps: int) -> dict:
         """Mean ms of each call (layout, dispatch, combine) with an event
-        between calls, so each includes its own launch."""
+        between calls, so each includes its own launch.  Each call finds in
+        L2 what the call before it left there: the combine, for one, writes
+        back the dispatch's dirty lines as it evicts them."""
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
         torch.cuda.synchronize()
         for e in evs:
@@ -544,11 +546,29 @@ class Prepared:
         return {nm: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
                 for j, nm in enumerate(KERNEL_NAMES)}
 
+    def time_kernels_clean_l2(self, steps: int) -> dict:
+        """The same calls, each after a read of a buffer twice the L2's size
+        (untimed), so each starts on a clean, cold L2: no dirty lines of the
+        call before it to write back, no input of its own in L2."""
+        flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.int32, device=self.x.device).fill_(1)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+        torch.cuda.synchronize()
+        for e in evs:
+            for j, call in enumerate((self.layout, self.dispatch, self.combine)):
+                flush.max()
+                e[2 * j].record(self.stream)
+                call()
+                e[2 * j + 1].record(self.stream)
+        torch.cuda.synchronize()
+        del flush
+        return {nm: statistics.mean(e[2 * j].elapsed_time(e[2 * j + 1]) for e in evs)
+                for j, nm in enumerate(KERNEL_NAMES)}
+
 
 KERNEL_NAMES = ("layout", "dispatch", "combine")
 
 
-def kernel_entries(cfg, n_rows, per_kernel_ms, peak, peak_kind) -> dict:
+def kernel_entries(cfg, n_rows, per_kernel_ms, peak, peak_kind, clean_ms=None) -> dict:
     abytes = algorithmic_bytes(cfg, n_rows)
     out = {}
     for nm in KERNEL_NAMES:
@@ -556,6 +576,10 @@ def kernel_entries(cfg, n_rows, per_kernel_ms, peak, peak_kind) -> dict:
         gbs = abytes[nm] / (us * 1e-6) / 1e9
         out[nm] = {"us": round(us, 2), "kernel": kernel_symbol(nm, cfg), "algorithmic_bytes": abytes[nm],
                    "gbs": round(gbs, 1), "frac_of_" + peak_kind + "_peak": round(gbs / peak, 4)}
+        if clean_ms is not None:
+            cus = clean_ms[nm] * 1e3
+            out[nm]["us_clean_l2"] = round(cus, 2)
+            out[nm]["frac_clean_l2"] = round(abytes[nm] / (cus * 1e-6) / 1e9 / peak, 4)
     return out
 
 
@@ -568,12 +592,13 @@ def measure_workload(cfg: W.EPConfig, dev, peak: float, peak_kind: str, steps: i
         pw.step()
     step_ms = pw.time_steps(steps)
     per = pw.time_kernels(min(steps, 200))
+    clean = pw.time_kernels_clean_l2(min(steps, 100))
     assert pw.lay.errors() == 0
     abytes = algorithmic_bytes(cfg, pw.n_rows)
     step_gbs = sum(abytes.values()) / (step_ms * 1e-3) / 1e9
     res = {"recv_rows": pw.n_rows, "step_us": round(step_ms * 1e3, 2),
            "step_frac_of_" + peak_kind + "_peak": round(step_gbs / peak, 4),
-           "kernels": kernel_entries(cfg, pw.n_rows, per, peak, peak_kind),
+           "kernels": kernel_entries(cfg, pw.n_rows, per, peak, peak_kind, clean),
            "steps": steps, "l2": l2_note(cfg, pw.n_rows)}
     del pw
     torch.cuda.empty_cache()
@@ -614,17 +639,22 @@ def run_ours(args, rank, world, local):
 
         # (2) the same steps with an event between calls: per-call durations.
         per_kernel_ms = pw.time_kernels(min(args.steps, 500))
+        clean_ms = pw.time_kernels_clean_l2(min(args.steps, 200))
         assert pw.lay.errors() == 0
 
         peak, peak_kind = hbm_peak()
         abytes = algorithmic_bytes(cfg, n_rows)
-        kernels = kernel_entries(cfg, n_rows, per_kernel_ms, peak, peak_kind)
+        kernels = kernel_entries(cfg, n_rows, per_kernel_ms, peak, peak_kind, clean_ms)
         dom = max(KERNEL_NAMES, key=lambda nm: per_kernel_ms[nm])
         dom_gbs = abytes[dom] / (per_kernel_ms[dom] * 1e-3) / 1e9
         roofline = {"bound": "hbm", "kernel": kernel_symbol(dom, cfg), "achieved": round(dom_gbs, 1),
                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                     "frac": round(dom_gbs / peak, 4), "traffic": ncu_traffic(dom, cfg),
-                    "algorithmic_bytes_per_launch": abytes[dom]}
+                    "algorithmic_bytes_per_launch": abytes[dom],
+                    "frac_clean_l2": kernels[dom]["frac_clean_l2"],
+                    "note": "achieved: in sequence after the dispatch, whose dirty L2 lines this kernel "
+                            "writes back as it evicts them; frac_clean_l2: the same call after an L2 "
+                            "flush by a read"}
         step_bytes = sum(abytes.values())
         step_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
 

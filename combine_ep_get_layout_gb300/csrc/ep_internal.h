@@ -121,7 +121,7 @@ struct DispatchArgs {
   int32_t *num_tokens_per_rank = nullptr;
 };
 // early_rows of ep_get_layout_and_dispatch (the input stages and the output
-// buffers of the warp-specialised kernel hold up to 5 tokens)
+// buffers of the warp-specialised kernel hold up to 4 tokens)
 constexpr int kEarlyRows = 3;
 // bf16 rows of the rank path through the warp-specialised kernel (else the
 // ring kernel); the one-launch layout of ep_get_layout_and_dispatch needs it
