@@ -304,14 +304,17 @@ ep_status_t ep_dispatch_ex(const ep_dispatch_args_t *args, ep_stream_t stream);
  * the layout, which writes nothing the dispatch reads first, so each
  * dispatch block loads (and for fp8 casts) the rows of its first tokens
  * while the layout still runs, and waits for it only to store them.  With
- * 0 < T <= 524,288 the layout is one launch: it writes
- * is_token_in_rank, rank_prefix, num_tokens_per_rank and each slot relative
- * to its block of 256 tokens, and the dispatch adds each block's base as it
- * moves the token, writes the final slot back and counts
- * num_tokens_per_expert (and bad ids).  Every output of both calls is
- * written, identical to the two calls (on that path, if the dispatch gives
- * up with EP_ERRBIT_TIMEOUT, the tokens it did not reach keep their
- * block-relative slots and are not counted).
+ * 0 < T <= 524,288 the layout is one launch: it writes is_token_in_rank,
+ * each slot relative to its block of 256 tokens and each block's per-rank
+ * totals.  When the blocks times the ranks number at most 1024, the
+ * dispatch itself scans those totals into each block's base and writes
+ * rank_prefix and num_tokens_per_rank; beyond that, the layout's last block
+ * to finish does the scan.  The dispatch adds each block's base as it moves
+ * the token, writes the final slot back and counts num_tokens_per_expert
+ * (and bad ids).  Every output of both calls is written, identical to the
+ * two calls (on that path, if the dispatch gives up with
+ * EP_ERRBIT_TIMEOUT, the tokens it did not reach keep their block-relative
+ * slots and are not counted).
  *   args       as for ep_dispatch_ex; every array of *args->layout is
  *              written (as ep_get_layout), so its token_slot and
  *              is_token_in_rank must be 16-byte aligned.
