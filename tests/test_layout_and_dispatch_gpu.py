@@ -116,6 +116,7 @@ CASES = [
     ("bf16_table_R64_1024_totals", 16 * 256, 128, 8, 128, 64, "bf16", {}),
     ("bf16_scan_R64_1088_totals", 16 * 256 + 1, 128, 8, 128, 64, "bf16", {}),
     ("bf16_table_R3_ragged", 300 * 256 + 17, 64, 3, 12, 3, "bf16", {}),
+    ("bf16_table_R1_1024_totals", 1024 * 256, 64, 2, 4, 1, "bf16", {}),
 ]
 
 
