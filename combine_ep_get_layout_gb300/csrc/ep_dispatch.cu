@@ -59,9 +59,10 @@ struct DispatchParams {
   uint32_t out_stride;     // fp8 output row, H rounded up to 128
   uint32_t scale_stride;   // fp8 scales of one row, groups*4 rounded up to 16
   TokenSource tokens;      // the order in which blocks take tokens
-  int early;               // fp8 kernel: rows loaded and cast before the wait for the previous kernel
-  // fp8 kernel after the local layout: token_slot holds block-relative slots;
-  // slot = relative + local_base[(t / 256) * R + r], written to token_slot_out
+  int early;               // rows loaded (and cast) before the wait for the previous kernel
+  // warp-specialised kernels after the local layout: token_slot holds
+  // block-relative slots; slot = relative + the block's base (local_base[(t /
+  // 256) * R + r], or from the scanned table), written to token_slot_out
   const int32_t *local_base;
   int32_t *token_slot_out;
   int32_t *num_tokens_per_expert;

@@ -104,8 +104,9 @@ struct DispatchArgs {
   float *recv_topk_weights;
   int recv_capacity;
   uint32_t *recv_stats;  // [E] or null
-  // fp8 rows: tokens per block loaded and cast before the wait for the
-  // previous kernel on the stream; only when that kernel writes none of x
+  // warp-specialised kernels: tokens per block loaded (and for fp8 cast)
+  // before the wait for the previous kernel on the stream; only when that
+  // kernel writes none of x
   int early_rows = 0;
   // after launch_layout_local: token_slot holds slots relative to each
   // 256-token block; the dispatch adds the block's base, writes the slot back
