@@ -79,11 +79,22 @@ def kernel_symbol(kernel: str, cfg: W.EPConfig) -> str:
     return "combine_ws_kernel" if cfg.num_ranks <= 8 else "combine_kernel"
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and blank space, so that editing a
+    comment does not mark a kernel as changed."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(kernel: str) -> str:
+    """A hash of the code of the sources a kernel is built from (comments
+    and layout ignored)."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "combine_ep_get_layout_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "combine_ep_get_layout_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
