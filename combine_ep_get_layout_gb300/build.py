@@ -1,10 +1,14 @@
 """Builds ``libep_gb300.so`` (the C-ABI library) from ``csrc/`` with nvcc.
 
-    python -m combine_ep_get_layout_gb300.build [--force] [--verbose]
+    python -m combine_ep_get_layout_gb300.build [--force] [--verbose] [--trace]
 
 One ``-gencode arch=compute_103a,code=sm_103a`` target, translation units
 compiled in parallel, objects under ``_build/`` beside this file, the shared
 library beside this file.  Nothing is installed anywhere else.
+
+``--trace`` builds ``libep_gb300_trace.so`` instead: the same sources with
+``EP_TRACE`` defined, so the kernels record per-block timeline marks (see
+``csrc/ep_trace.cuh`` and ``trace.py``).  The product library never has them.
 """
 from __future__ import annotations
 
@@ -24,7 +28,8 @@ LIB = os.path.join(HERE, "libep_gb300.so")
 
 SOURCES = ["ep_api.cu", "ep_layout.cu", "ep_layout_expanded.cu", "ep_dispatch.cu", "ep_combine.cu",
            "ep_noalloc.cu", "ep_selftest.cu"]
-HEADERS = ["ep_device.cuh", "ep_internal.h"]
+HEADERS = ["ep_device.cuh", "ep_internal.h", "ep_trace.cuh"]
+TRACE_LIB = os.path.join(HERE, "libep_gb300_trace.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
          "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr"]
@@ -42,23 +47,28 @@ def _inputs() -> list[str]:
             + [os.path.join(INCLUDE, "ep_gb300.h"), os.path.abspath(__file__)])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile the library if a source is newer than it; return its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, trace: bool = False) -> str:
+    """Compile the library (or with ``trace`` the trace build) if a source
+    is newer than it; return its path."""
+    lib = TRACE_LIB if trace else LIB
+    if not force and up_to_date(lib):
+        return lib
+    build_dir = os.path.join(BUILD, "trace") if trace else BUILD
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if trace:
+        extra.append("-DEP_TRACE")
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         p = subprocess.run(cmd, capture_output=True, text=True)
         if p.returncode != 0:
@@ -69,13 +79,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     p = subprocess.run(cmd, capture_output=True, text=True)
     if p.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{' '.join(cmd)}\n{p.stdout}\n{p.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 def main(argv=None) -> int:
@@ -83,8 +93,9 @@ def main(argv=None) -> int:
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
     ap.add_argument("--ptxas-info", action="store_true", help="print registers / spills / smem")
+    ap.add_argument("--trace", action="store_true", help="the trace build (per-block timeline marks)")
     a = ap.parse_args(argv)
-    print(build(force=a.force, verbose=a.verbose, ptxas_info=a.ptxas_info))
+    print(build(force=a.force, verbose=a.verbose, ptxas_info=a.ptxas_info, trace=a.trace))
     return 0
 
 

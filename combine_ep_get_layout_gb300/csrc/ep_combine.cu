@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "ep_device.cuh"
+#include "ep_trace.cuh"
 
 namespace ep {
 namespace {
@@ -256,6 +257,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
 // header flagged, and the reducers carry the partial sum from the first in
 // registers (rows stay in ascending rank order, so the sum is unchanged).
 
+// Trace build only (warp-specialised kernel): 0 entry, 1 past the wait for
+// the kernel ahead, 2 the loader's first token drawn, 3 the reducers' first
+// rows in, 4 the loader draws the end, 5 the reducers done, 6 (a count) the
+// loader's draws.
+EP_TRACE_ARRAY(g_trace_combine);
+
 constexpr int kWsMaxRanks = 8;
 constexpr int kSmallStageRows = 6;
 constexpr int kSplitMinTokens = 32768;
@@ -305,6 +312,7 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
   const int warp = tid / kWarpSize;
   const int lane = tid & (kWarpSize - 1);
   const int nchunk = (p.H + kChunk - 1) / kChunk;  // a CTA takes all chunks of a token in a row
+  if (tid == 0) EP_TRACE_MARK(g_trace_combine, 0);
 
   if (tid == 0) {
     for (int s = 0; s < kCombineStages; ++s) {
@@ -339,6 +347,7 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
   }
   griddep_wait();
   griddep_launch_dependents();
+  if (tid == 0) EP_TRACE_MARK(g_trace_combine, 1);
 
   const uint32_t lanes_below = (1u << lane) - 1u;
   long loads_issued = 0;  // loader lane 0: units issued (loads and the end)
@@ -351,10 +360,15 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
     };
     long i = 0;  // unit counter: stage i % kCombineStages
     int t = draw(0);
+    if (lane == 0) EP_TRACE_MARK(g_trace_combine, 2);
     TokenMeta cur = t >= 0 ? fetch_meta(p, t, lane, WEIGHTED) : TokenMeta{-1, -1, 0.0f};
     bool ok = true;
     for (int j = 1; ok && !*s_abort; ++j) {
       if (t < 0) {  // the end: a unit with n = -1 tells the reducers
+        if (lane == 0) {
+          EP_TRACE_MARK(g_trace_combine, 4);
+          EP_TRACE_VALUE(g_trace_combine, 6, j);
+        }
         const int s = static_cast<int>(i % kCombineStages);
         if (i >= kCombineStages)
           ok = __all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], (uint32_t)(i / kCombineStages - 1) & 1u));
@@ -463,6 +477,7 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
         }
         const int *hdr = reinterpret_cast<const int *>(stage);
         const int nrows = hdr[0];
+        if (rt == 0 && i == 0) EP_TRACE_MARK(g_trace_combine, 3);
         if (nrows < 0) {  // the end
           more = false;
           break;
@@ -532,6 +547,7 @@ __global__ void __launch_bounds__(kWsCombineThreads) combine_ws_kernel(CombinePa
     }
   }
 
+  if (tid == kWarpSize) EP_TRACE_MARK(g_trace_combine, 5);
   // After an abort, the loads of the latest units still in flight are
   // waited for (bounded) before the CTA's shared memory is released.
   __syncthreads();
@@ -629,3 +645,5 @@ ep_status_t launch_combine(const CombineArgs &a, cudaStream_t stream) {
 }
 
 }  // namespace ep
+
+EP_TRACE_READER(ep_trace_read_combine, ep::g_trace_combine);

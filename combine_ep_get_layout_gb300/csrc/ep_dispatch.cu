@@ -21,6 +21,7 @@
 #include <mutex>
 
 #include "ep_device.cuh"
+#include "ep_trace.cuh"
 
 namespace ep {
 namespace {
@@ -451,6 +452,11 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_ring_kernel(Dispatc
 // no casters: the storer stores each row from its input stage and releases
 // the stage (empty_in) one token late, once those stores have read it.
 
+// Trace build only (warp-specialised kernels): 0 entry, 1 the storer past
+// its wait for the kernel ahead (and the table scan), 2 its first token, 4 it
+// sees the end, 5 its stores done, 6 (a count) the tokens it stored.
+EP_TRACE_ARRAY(g_trace_dispatch);
+
 constexpr int kWsCasters = 8;
 constexpr int kWsThreads = (2 + kWsCasters) * kWarpSize;
 constexpr int kWsBf16Threads = 2 * kWarpSize;  // loader and storer
@@ -509,6 +515,7 @@ __device__ __forceinline__ void dispatch_ws_body(const DispatchParams &p) {
   const int warp = tid / kWarpSize;
   const int lane = tid & (kWarpSize - 1);
 
+  if (tid == 0) EP_TRACE_MARK(g_trace_dispatch, 0);
   if (tid < kTokRing) s_tok[tid] = kTokPending;
   if (tid == 0) *s_stored = 0;
   if (tid == 0) {
@@ -607,6 +614,7 @@ __device__ __forceinline__ void dispatch_ws_body(const DispatchParams &p) {
         }
       }
     }
+    if (lane == 0) EP_TRACE_MARK(g_trace_dispatch, 1);
     for (int i = 0; !*s_abort; ++i) {
       if (lane == 0) *s_stored = i;  // tokens before i are stored
       const int t = wait_token(&s_tok[i % kTokRing]);
@@ -617,7 +625,14 @@ __device__ __forceinline__ void dispatch_ws_body(const DispatchParams &p) {
         }
         break;
       }
-      if (t < 0) break;
+      if (t < 0) {
+        if (lane == 0) {
+          EP_TRACE_MARK(g_trace_dispatch, 4);
+          EP_TRACE_VALUE(g_trace_dispatch, 6, i);
+        }
+        break;
+      }
+      if (i == 0 && lane == 0) EP_TRACE_MARK(g_trace_dispatch, 2);
       if (t >= p.T) {  // a hand-over that went wrong: stop, do not index with it
         if (lane == 0) {
           *s_abort = 1;
@@ -751,6 +766,7 @@ __device__ __forceinline__ void dispatch_ws_body(const DispatchParams &p) {
       release_out(empty_out, i, lane);
     }
     bulk_wait<0>();
+    if (lane == 0) EP_TRACE_MARK(g_trace_dispatch, 5);
   } else if (CAST) {
     const int cw = warp - 2;
     for (int i = 0; !*s_abort; ++i) {
@@ -1063,3 +1079,5 @@ ep_status_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream) {
 }
 
 }  // namespace ep
+
+EP_TRACE_READER(ep_trace_read_dispatch, ep::g_trace_dispatch);

@@ -25,6 +25,7 @@
 #include <algorithm>
 
 #include "ep_device.cuh"
+#include "ep_trace.cuh"
 
 namespace ep {
 namespace {
@@ -33,6 +34,11 @@ constexpr int kLayoutThreads = 256;  // one token per thread per chunk
 constexpr int kLayoutWarps = kLayoutThreads / kWarpSize;
 constexpr size_t kPartialOffset = 256;  // workspace header (the local layout's ticket word), then the totals
 constexpr int kMaxLayoutBlocks = 2048;  // more tokens per block beyond this
+
+// Trace build only: 0 entry, 1 the wait for the kernel ahead done, 2 ids
+// loaded, 3 totals published, 5 slots written, 6 (last block) totals read,
+// 7 (last block) bases written.
+EP_TRACE_ARRAY(g_trace_layout);
 
 struct LayoutParams {
   const int64_t *topk_idx;
@@ -287,9 +293,11 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_local_kernel(LayoutPara
   const int G = gridDim.x;
   const int b = blockIdx.x;
   const int R = p.num_ranks, E = p.num_experts;
+  if (tid == 0) EP_TRACE_MARK(g_trace_layout, 0);
   prefetch_ids(p, b * kLayoutThreads, min(kLayoutThreads, p.num_tokens - b * kLayoutThreads));
   griddep_wait();
   griddep_launch_dependents();
+  if (tid == 0) EP_TRACE_MARK(g_trace_layout, 1);
   if (b == 0) {  // the dispatch adds into them, after this kernel
     for (int i = tid; i < E; i += kLayoutThreads) p.out.num_tokens_per_expert[i] = 0;
     if (tid == 0) *p.out.error_word = 0u;
@@ -300,6 +308,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_local_kernel(LayoutPara
   load_ids(p, t, p.num_tokens, ids);
   bool bad = false;  // the dispatch reports bad ids
   const uint64_t mask = rank_mask(ids, p.num_topk, E, p.experts_per_rank, nullptr, bad);
+  if (tid == 0 && mask != ~0ull) EP_TRACE_MARK(g_trace_layout, 2);  // once the ids are in
   for (int r = 0; r < R; ++r) {
     const uint32_t bal = __ballot_sync(0xffffffffu, (mask >> r) & 1ull);
     if (lane == 0) warp_off[warp * R + r] = __popc(bal);
@@ -320,6 +329,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_local_kernel(LayoutPara
   // writes.
   if constexpr (SCAN) __threadfence();
   __syncthreads();
+  if (tid == 0) EP_TRACE_MARK(g_trace_layout, 3);
   if (SCAN && tid == 0) s_last = atomicAdd(done, 1u) == (uint32_t)G - 1u;
   const uint32_t lanes_below = (1u << lane) - 1u;
   const bool vec4 = (R % 4) == 0;
@@ -351,6 +361,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_local_kernel(LayoutPara
       }
     }
   }
+  if (tid == 0) EP_TRACE_MARK(g_trace_layout, 5);
   if constexpr (!SCAN) return;
 
   // The last block: bases.  Thread (q, r) owns a contiguous run of blocks
@@ -369,6 +380,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_local_kernel(LayoutPara
     seg_sum[tid] = sum;
   }
   __syncthreads();
+  if (tid == 0) EP_TRACE_MARK(g_trace_layout, 6);
   for (int rr = tid; rr < R; rr += kLayoutThreads) {
     int all = 0;
     for (int qq = 0; qq < per_rank; ++qq) all += seg_sum[qq * R + rr];
@@ -398,6 +410,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_local_kernel(LayoutPara
     }
   }
   if (tid == 0) *done = 0u;
+  if (tid == 0) EP_TRACE_MARK(g_trace_layout, 7);
 }
 
 int max_layout_blocks(int num_tokens) {
@@ -481,3 +494,5 @@ ep_status_t launch_layout_local(const int64_t *topk_idx, int num_tokens, int num
 }
 
 }  // namespace ep
+
+EP_TRACE_READER(ep_trace_read_layout, ep::g_trace_layout);

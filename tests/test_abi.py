@@ -407,3 +407,16 @@ def test_a_c99_program_links_and_calls_the_library(lib, tmp_path):
     out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
     # 256 header bytes + one int32 total per (256-token block, rank)
     assert out == [str(256 + (8192 // 256) * 8 * 4), "EP_ERR_INVALID_ARG", "1"]
+
+
+def test_trace_build_is_separate():
+    """The product library has no trace marks; the trace build (EP_TRACE)
+    compiles from the same sources and exports its three readers."""
+    from combine_ep_get_layout_gb300 import build, _native
+    lib = _native.load()
+    for name in ("ep_trace_read_layout", "ep_trace_read_dispatch", "ep_trace_read_combine"):
+        assert not hasattr(lib, name), name
+    tlib = C.CDLL(build.build(trace=True))
+    for name in ("ep_trace_read_layout", "ep_trace_read_dispatch", "ep_trace_read_combine"):
+        assert hasattr(tlib, name), name
+    assert set(declared_functions()) <= {n for n in declared_functions() if hasattr(tlib, n)}
