@@ -626,14 +626,15 @@ def run_ours(args, rank, world, local):
         pw = Prepared(cfg, dev, inp=inp, y_np=y_np)
         n_rows = pw.n_rows
 
-        for _ in range(args.warmup):
-            pw.step()
-        torch.cuda.synchronize()
-
         # (1) K steps, bracketed by barrier + synchronize, timed on the stream.
+        # The W warm-up steps run right before them, once the clock sampler
+        # has started (its start leaves the GPU idle for a moment, which a
+        # short timed region would otherwise begin with).
         stream = pw.stream
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with ClockSampler(gpu_index_for_smi(local)) as clocks:
+            for _ in range(args.warmup):
+                pw.step()
             barrier(world)
             torch.cuda.synchronize()
             t_wall = time.perf_counter()
