@@ -15,7 +15,14 @@ better), device-timed with CUDA events on the launching stream, inputs
 resident in HBM.  Each step's working set (~1.2 GB) is far larger than the
 129 MB L2, so no step reuses another's data from L2 and no flush is done.
 `e2e` times the same step through the public binding with the inputs copied
-from pinned host memory and the combined output copied back, every step.
+from pinned host memory and the combined output copied back, every step,
+beside the same copies alone (the host link's bound).  `kernels` gives each
+call's time with an event between the calls (in sequence, each finding in
+L2 what the call before it left) and after an L2 flush (`us_clean_l2`);
+`roofline` is the dominant kernel's; `workloads` repeats the step and the
+per-call times for every workload of `workloads.py`; `cpu_baseline` is the
+oracle on the whole workload on all host cores and on one; `gpu_processes`
+samples `nvidia-smi pmon` over the run (`foreign_sm_use`).
 `--impl reference` times the CPU oracle (the plain C restatement of the
 method) on the host cores instead.  Under torchrun each rank runs an
 independent replica on its own GPU (the path has no cross-GPU exchange on
