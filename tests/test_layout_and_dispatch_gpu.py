@@ -268,3 +268,33 @@ def test_rows_made_by_a_kernel_just_before_each_call():
     U.assert_layout_equal(U.layout_np(lay), lo)
     for i in range(calls):
         U.assert_dispatch_equal(U.dispatch_np(outs[i]), want[i % 3], N, True)
+
+
+def test_one_layout_object_across_sizes_and_modes():
+    """One layout object and workspace (sized for the largest call) reused by
+    one-call layouts of changing sizes, alternating between the table mode
+    (the dispatch scans the block totals) and the scan mode (the layout's last
+    block does, with its ticket word): every call's layout and rows against
+    the oracle, and the ticket word and work counters left at zero."""
+    E, R, K, H = 64, 8, 6, 256
+    sizes = [100, 40_000, 8192, 1, 300_000, 33_000, 256, 40_000, 4097]
+    rng = np.random.default_rng(31)
+    big = max(sizes)
+    lay_big = ep.Layout.empty(big, E, R, U.dev())
+    for T in sizes:
+        idx, w, _ = _routing(T, K, E, T % 1000)
+        x = W.normal_bf16(rng, (T, H))
+        lo = oracle.get_layout(idx, E, R)
+        N = int(lo["rank_prefix"][R])
+        want = oracle.dispatch(x, idx, w, E, R, lo["token_slot"], True, max(N, 1))
+        lay = ep.Layout.empty(T, E, R, U.dev())
+        lay.workspace = lay_big.workspace
+        lay.work_counters = lay_big.work_counters
+        lay, d = ep.ep_get_layout_and_dispatch(U.to_dev_bf16(x), torch.from_numpy(idx).to(U.dev()),
+                                               torch.from_numpy(w).to(U.dev()), E, R, layout=lay, dtype="fp8",
+                                               recv_capacity=max(N, 1))
+        torch.cuda.synchronize()
+        U.assert_layout_equal(U.layout_np(lay), lo)
+        U.assert_dispatch_equal(U.dispatch_np(d), want, N, True)
+        assert U.bits(lay_big.work_counters).tolist() == [0, 0, 0, 0], T
+        assert int(lay_big.workspace[:4].view(torch.int32).item()) == 0, T  # the scan mode's ticket word
