@@ -87,11 +87,14 @@ def kernel_symbol(kernel: str, cfg: W.EPConfig) -> str:
 
 
 def _code_only(text: str) -> str:
-    """C++ source without comments and blank space, so that editing a
-    comment does not mark a kernel as changed."""
+    """C++ source without comments, blank space and the trace build's marks
+    (lines naming an EP_TRACE_ macro, which compile to nothing in the
+    product library), so that editing a comment or a trace point does not
+    mark a kernel as changed."""
     import re
     text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
     text = re.sub(r"//[^\n]*", " ", text)
+    text = "\n".join(line for line in text.splitlines() if "EP_TRACE_" not in line)
     return " ".join(text.split())
 
 

@@ -30,7 +30,8 @@ from . import build as B
 SLOTS = 8
 # the points each kernel marks (slot: name), as the kernels' trace comments list them
 LAYOUT_POINTS = {0: "entry", 1: "wait_done", 2: "ids_loaded", 3: "totals_published", 5: "slots_written"}
-DISPATCH_POINTS = {0: "entry", 1: "storer_ready", 2: "first_token", 4: "end_seen", 5: "stores_done"}
+DISPATCH_POINTS = {0: "entry", 7: "loader_wait_done", 3: "storer_wait_done", 1: "storer_ready", 2: "first_token",
+                   4: "end_seen", 5: "stores_done"}
 COMBINE_POINTS = {0: "entry", 1: "wait_done", 2: "first_token", 3: "first_rows_in", 4: "end_drawn",
                   5: "reducers_done"}
 

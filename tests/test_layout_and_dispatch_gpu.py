@@ -116,6 +116,10 @@ CASES = [
     ("bf16_table_R64_1024_totals", 16 * 256, 128, 8, 128, 64, "bf16", {}),
     ("bf16_scan_R64_1088_totals", 16 * 256 + 1, 128, 8, 128, 64, "bf16", {}),
     ("bf16_table_R3_ragged", 300 * 256 + 17, 64, 3, 12, 3, "bf16", {}),
+    # the table comes in by one bulk copy of its whole 16-byte groups, the
+    # words past them by loads: 18 totals (64 bytes + 2 words), 70 (272 + 2)
+    ("fp8_table_R3_bulk_and_tail", 5 * 256 + 9, 256, 3, 12, 3, "fp8", {}),
+    ("fp8_table_R7_bulk_and_tail", 2500, 384, 4, 28, 7, "fp8", {}),
     ("bf16_table_R1_1024_totals", 1024 * 256, 64, 2, 4, 1, "bf16", {}),
 ]
 
