@@ -58,13 +58,15 @@ def test_trace_marks_and_outputs(name):
     lay, disp, comb = r["layout"], r["dispatch"], r["combine"]
     # every block of every kernel reached its points in order (percentiles over blocks)
     for k, pts in ((lay, ["entry", "wait_done", "ids_loaded", "totals_published", "slots_written"]),
-                   (disp, ["entry", "storer_ready", "stores_done"]),
+                   (disp, ["entry", "storer_wait_done", "storer_ready", "stores_done"]),
+                   (disp, ["entry", "loader_wait_done"]),
                    (comb, ["entry", "wait_done", "first_rows_in", "reducers_done"])):
         for a, b in zip(pts, pts[1:]):
             assert k[a][0] <= k[b][0] and k[a][4] <= k[b][4], (a, b, k[a], k[b])
     # the kernel boundaries: the layout's wait ends after the combine ahead has finished ...
     assert lay["wait_done"][0] >= 0.0, lay["wait_done"]
-    # ... and the dispatch's storers start once the layout kernel has written its slots
-    assert disp["storer_ready"][0] >= lay["slots_written"][4], (disp["storer_ready"], lay["slots_written"])
+    # ... and the dispatch's waits for the layout kernel end after its last block wrote its slots
+    for pt in ("storer_wait_done", "loader_wait_done", "storer_ready"):
+        assert disp[pt][0] >= lay["slots_written"][4], (pt, disp[pt], lay["slots_written"])
     assert comb["reducers_done"][4] == 0.0
     assert disp["tokens_per_block"][4] >= 1 and comb["draws_per_block"][4] >= 1
