@@ -479,12 +479,13 @@ constexpr size_t kWsBf16SmemBudget = 64 * 1024;
 // Two output buffers: measured against three, the headline step -1.3 us (the
 // same 4 blocks per SM, 15 KB less shared memory per SM in use).
 constexpr int kWsOut = 2;
-// fp8 rows: once a block has drawn one of the last kNearEndBlocks * gridDim.x
-// tokens, its loader draws the next token only when the storer is at most
-// one token behind, so the last tokens go to blocks with little left in
-// their pipelines and the grid's blocks finish closer together (measured:
-// headline step -1.2 us, 65 536 tokens -0.7 us; bf16 rows, with no casters,
-// were slower with it and keep the full pipeline).
+// Once a block has drawn one of the last kNearEndBlocks * gridDim.x tokens,
+// its loader draws the next token only when the storer is at most one token
+// behind, so the last tokens go to blocks with little left in their
+// pipelines and the grid's blocks finish closer together (measured: fp8
+// rows, headline step -1.2 us, 65 536 tokens -0.7 us; bf16 rows, whose
+// loader otherwise runs up to seven stages ahead, bf16 step -0.45 us and
+// skewed -0.3 us, two tokens ahead timing the same).
 constexpr int kNearEndBlocks = 2;
 // The storer releases an output buffer one token late (once the next
 // token's stores are issued), so waiting for the stores to read a buffer
@@ -586,7 +587,7 @@ __device__ __forceinline__ void dispatch_ws_body(const DispatchParams &p) {
           set_error(p.error_word, EP_ERRBIT_TIMEOUT);
           break;
         }
-        if (CAST && near_end && i >= 1) {  // at most one token ahead of the storer (bounded wait)
+        if (near_end && i >= 1) {  // at most one token ahead of the storer (bounded wait)
           const uint64_t t0 = global_timer_ns();
           while (*s_stored < i - 1 && !*s_abort) {
             if (global_timer_ns() - t0 > kWaitLimitNs) {
