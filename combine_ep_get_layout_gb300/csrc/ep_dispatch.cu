@@ -169,7 +169,8 @@ __device__ __forceinline__ int local_expert(const DispatchParams &p, int64_t e) 
 // bulk copy (their 16-byte-aligned prefix, mbarrier `bar`, used once; the
 // few left over by plain loads): one round trip to L2 for the whole table
 // (measured: headline step -0.24 us against loads of four words a lane).
-// False if the copy did not land within the wait limit.
+// False if the copy did not land within the wait limit (after a second
+// bounded wait for it, so that the block does not exit with it in flight).
 __device__ __forceinline__ bool scan_block_totals(const int32_t *tot, int G, int R, int32_t *base, int32_t *rtot,
                                                   int32_t *roff, int lane, uint64_t *bar) {
   const int n = G * R;
@@ -193,6 +194,7 @@ __device__ __forceinline__ bool scan_block_totals(const int32_t *tot, int G, int
     }
   }
   const bool ok = __all_sync(0xffffffffu, !use_bulk || mbar_wait_bounded(bar, 0));
+  if (!ok && lane == 0) (void)mbar_wait_bounded(bar, 0);  // the copy still in flight: once more, bounded
   __syncwarp();
   if (!ok) return false;
   int rp = 1;
