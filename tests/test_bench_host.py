@@ -55,6 +55,19 @@ def test_traffic_lookup_needs_matching_source(tmp_path, monkeypatch):
     assert bench.ncu_traffic("combine", cfg.with_(name="other")) is None
 
 
+def test_source_hash_ignores_comments_and_trace_marks():
+    """The hash that keys the ncu traffic changes with the code the product
+    library compiles, not with comments or the trace build's marks (which
+    expand to nothing there)."""
+    code = "int f(int a) {\n  return a + 1;\n}\n"
+    noted = ("// a note\nint f(int a) {  /* block\n comment */\n"
+             "  if (a == 0) EP_TRACE_MARK(g_trace_x, 3);\n  return a + 1;\n}\n")
+    changed = "int f(int a) {\n  return a + 2;\n}\n"
+    assert bench._code_only(noted) == bench._code_only(code)
+    assert bench._code_only(changed) != bench._code_only(code)
+    assert len(bench.kernel_source_hash("combine")) == 16
+
+
 def _free_port():
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))
