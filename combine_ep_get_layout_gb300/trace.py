@@ -114,18 +114,26 @@ def timeline(workload: str, steps: int = 30, device: str = "cuda:0") -> dict:
         h.update(t.contiguous().view(torch.uint8).cpu().numpy().tobytes())
     res = {"workload": workload, "steps": steps, "unit": "us after the combine's last reducer finished",
            "outputs_sha256": h.hexdigest()[:16]}
-    traced = {}
-    for name, reader, points in (("layout", "ep_trace_read_layout", LAYOUT_POINTS),
-                                 ("dispatch", "ep_trace_read_dispatch", DISPATCH_POINTS),
-                                 ("combine", "ep_trace_read_combine", COMBINE_POINTS)):
-        a = _read(lib, reader, 4096)
-        traced[name] = a[a[:, 0] > 0]  # blocks that ran (the grid of the last launch)
+    res.update(summarize({name: _read(lib, reader, 4096) for name, reader in
+                          (("layout", "ep_trace_read_layout"), ("dispatch", "ep_trace_read_dispatch"),
+                           ("combine", "ep_trace_read_combine"))}))
+    return res
+
+
+def summarize(raw: dict) -> dict:
+    """Percentiles of each kernel's marks, from the three arrays as read
+    ([blocks, SLOTS] of ns): blocks whose entry slot is zero did not run in
+    the last launch; a mark older than its block's entry is a previous
+    launch's (the block skipped that point) and is left out.  Times are µs
+    after the combine's last reducer finished."""
+    traced = {name: a[a[:, 0] > 0] for name, a in raw.items()}
     t0 = int(traced["combine"][:, 5].max())
+    res = {}
     for name, points in (("layout", LAYOUT_POINTS), ("dispatch", DISPATCH_POINTS), ("combine", COMBINE_POINTS)):
         a = traced[name]
         res[name] = {"blocks": int(a.shape[0])}
         for slot, pt in points.items():
-            v = a[a[:, slot] >= a[:, 0], slot]  # marks of the last launch (a block may skip a point)
+            v = a[a[:, slot] >= a[:, 0], slot]
             res[name][pt] = _pct((v - t0) / 1e3) if v.size else None
     res["dispatch"]["tokens_per_block"] = _pct(traced["dispatch"][:, 6])
     res["combine"]["draws_per_block"] = _pct(traced["combine"][:, 6])
