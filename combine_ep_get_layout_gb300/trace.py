@@ -122,10 +122,11 @@ def timeline(workload: str, steps: int = 30, device: str = "cuda:0") -> dict:
 
 def summarize(raw: dict) -> dict:
     """Percentiles of each kernel's marks, from the three arrays as read
-    ([blocks, SLOTS] of ns): blocks whose entry slot is zero did not run in
-    the last launch; a mark older than its block's entry is a previous
-    launch's (the block skipped that point) and is left out.  Times are µs
-    after the combine's last reducer finished."""
+    ([blocks, SLOTS] of ns): blocks whose entry slot is zero never ran (the
+    arrays start at zero, and the launches of one workload have one grid);
+    a mark older than its block's entry is a previous launch's (the block
+    skipped that point) and is left out.  Times are µs after the combine's
+    last reducer finished."""
     traced = {name: a[a[:, 0] > 0] for name, a in raw.items()}
     t0 = int(traced["combine"][:, 5].max())
     res = {}
